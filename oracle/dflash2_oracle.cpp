@@ -1,0 +1,498 @@
+// dflash2_oracle.cpp -- TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+//
+// A plain, slow, obviously-correct CPU restatement of the DFlash 2 draft-block
+// head, written from "DFlash 2: Keep Drafting Parallel" (Inco AI).  Only the
+// test suite, the smoke check and the benchmark's CPU-baseline leg may load
+// this library.  It shares no code, header, table or helper with the CUDA
+// library; the two meet only through the seeded input generator, which holds
+// none of the method's arithmetic.
+//
+// Conventions
+//   * bf16 tensors arrive as raw uint16 bit patterns; they are widened exactly
+//     (bits << 16) to float and then to double.
+//   * Everything is accumulated in double unless a function says otherwise.
+//   * Loops follow the definitions directly: no blocking, fusion or reordering.
+//   * `nthreads` <= 1 runs single-threaded; larger values split the outermost
+//     loop over independent rows / sequences with OpenMP (results do not
+//     depend on the thread count: every row is computed by one thread).
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//   R1  top-16 order: value descending, ties by lowest vocabulary id; -0 == +0;
+//       NaN ranks below -inf.
+//   R2  context gate H(h_t) = sigmoid(W_H h_t + b_H), one 256-vector per position.
+//   R3  position t = 0 has a single predecessor, the last verified token; the 16
+//       rows of its 16x16 score block are identical.
+//   R4  greedy walk = myopic best successor at every step, lowest slot on ties.
+//   R5  sampled walk = softmax(S/T) over the 16 successors of the chosen
+//       predecessor, inverse CDF in slot order with a Philox4x32-10 uniform.
+//   R6  conv correction [c0; c1] = W_c h_t (+ b_c), linear, no activation;
+//       rows [0, d/16) give c0, rows [d/16, 2d/16) give c1; channel ch belongs
+//       to group ch/16; h defaults to the conv input x; no residual.
+//   R7  verification at T > 0 is standard speculative rejection sampling with
+//       proposal q = the walk's per-step 16-slot distribution (zero elsewhere).
+//   R8  Philox counter = (b, t | stream << 24, offset_lo, offset_hi),
+//       key = (seed_lo, seed_hi); a uniform is (x0 >> 8) * 2^-24.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+double widen_bf16(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+float widen_bf16_f(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+int threads_for(int nthreads) { return nthreads < 1 ? 1 : nthreads; }
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10, from Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers:
+// As Easy as 1, 2, 3" (SC'11): ten rounds of the 4x32 S-box/P-box round with
+// multipliers 0xD2511F53 and 0xCD9E8D57 and the Weyl key schedule
+// (0x9E3779B9, 0xBB67AE85).  The pages name no generator (reading R8).
+// ---------------------------------------------------------------------------
+void philox_round(uint32_t c[4], const uint32_t k[2]) {
+  const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c[0];
+  const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c[2];
+  const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+  const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+  const uint32_t n0 = hi1 ^ c[1] ^ k[0];
+  const uint32_t n2 = hi0 ^ c[3] ^ k[1];
+  c[0] = n0;
+  c[1] = lo1;
+  c[2] = n2;
+  c[3] = lo0;
+}
+
+void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+  uint32_t k[2] = {key[0], key[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += 0x9E3779B9u;
+      k[1] += 0xBB67AE85u;
+    }
+    philox_round(c, k);
+  }
+  for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+// Uniform in [0, 1) with 24 random bits (reading R8).
+double uniform24(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, uint64_t offset) {
+  const uint32_t ctr[4] = {static_cast<uint32_t>(b),
+                           static_cast<uint32_t>(t) | (stream << 24),
+                           static_cast<uint32_t>(offset),
+                           static_cast<uint32_t>(offset >> 32)};
+  const uint32_t key[2] = {static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+  uint32_t out[4];
+  philox4x32_10(ctr, key, out);
+  return static_cast<double>(out[0] >> 8) * (1.0 / 16777216.0);
+}
+
+// Reading R1: does (va, ia) come strictly before (vb, ib) in top-k order?
+bool ranks_before(double va, int64_t ia, double vb, int64_t ib) {
+  const bool na = std::isnan(va), nb = std::isnan(vb);
+  if (na != nb) return nb;  // the non-NaN one comes first
+  if (!na && va != vb) return va > vb;
+  return ia < ib;
+}
+
+int64_t clamp_id(int64_t id, int64_t V, int* flag) {
+  if (id < 0 || id >= V) {
+    if (flag) *flag = 1;
+    return id < 0 ? 0 : V - 1;
+  }
+  return id;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Philox4x32-10 block function, exported so tests can check it against the
+// published known-answer vectors.
+void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) {
+  philox4x32_10(ctr, key, out);
+}
+
+double oracle_uniform24(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, uint64_t offset) {
+  return uniform24(seed, b, t, stream, offset);
+}
+
+// ---------------------------------------------------------------------------
+// Stage 1: per-position top-k candidates.
+// "A Lightweight Path Selector": DFlash 2 keeps the top 16 candidates of the
+// drafter's own logits U_t at every block position instead of the top-1.
+// Definition: order all V entries of a row by reading R1 and keep the first k
+// (std::partial_sort with that comparator).
+// logits: [rows, ld] bf16 bits; vals/idx: [rows, k].
+// ---------------------------------------------------------------------------
+void oracle_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, int k,
+                 float* vals, int32_t* idx, int nthreads) {
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads_for(nthreads))
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* row = logits + r * ld;
+    std::vector<int64_t> order(static_cast<size_t>(V));
+    for (int64_t v = 0; v < V; ++v) order[v] = v;
+    std::partial_sort(order.begin(), order.begin() + k, order.end(),
+                      [row](int64_t a, int64_t b) {
+                        return ranks_before(widen_bf16(row[a]), a, widen_bf16(row[b]), b);
+                      });
+    for (int j = 0; j < k; ++j) {
+      vals[r * k + j] = widen_bf16_f(row[order[j]]);
+      idx[r * k + j] = static_cast<int32_t>(order[j]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2a: context gate (reading R2), "A Lightweight Path Selector":
+// H(h_t) decides which parts of the embedding match count.
+// H[m, q] = 1 / (1 + exp(-(sum_k W_H[q, k] h[m, k] + b_H[q]))), in double.
+// h: [M, d] bf16; W_H: [r, d] bf16; b_H: [r] fp32 or null; H: [M, r] double.
+// ---------------------------------------------------------------------------
+void oracle_gate(const uint16_t* h, const uint16_t* W_H, const float* b_H, int64_t M,
+                 int64_t d, int64_t r, double* H, int nthreads) {
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t q = 0; q < r; ++q) {
+      double acc = b_H ? static_cast<double>(b_H[q]) : 0.0;
+      for (int64_t kk = 0; kk < d; ++kk)
+        acc += widen_bf16(W_H[q * d + kk]) * widen_bf16(h[m * d + kk]);
+      H[m * r + q] = 1.0 / (1.0 + std::exp(-acc));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2b: pairwise path-selector scores, "A Lightweight Path Selector",
+// score equation S_t(a, b) = U_t(b) + <A(a) (.) H(h_t), B(b)>:
+//   S[b, t, i, j] = U_t(c_t[j]) + sum_q A[p_i, q] * H[b, t, q] * B[c_t[j], q]
+// with p_i = c_{t-1}[i] for t >= 1 and p = last_verified[b] for t = 0
+// (reading R3).  U_t(c_t[j]) is cand_val[b, t, j].
+// cand_idx/cand_val: [B, L, K]; H: [B, L, r] double; A, Bt: [V, r] bf16;
+// S: [B, L, K, K] double.  Out-of-range ids are clamped and reported.
+// Returns 1 if any id was out of range, else 0.
+// ---------------------------------------------------------------------------
+int oracle_pair_scores(const int32_t* cand_idx, const float* cand_val,
+                       const int32_t* last_verified, const double* H, const uint16_t* A,
+                       const uint16_t* Bt, int64_t B, int64_t L, int64_t K, int64_t r,
+                       int64_t V, double* S, int nthreads) {
+  int any_bad = 0;
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads)) reduction(| : any_bad)
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t t = 0; t < L; ++t) {
+      const double* Ht = H + (b * L + t) * r;
+      for (int64_t i = 0; i < K; ++i) {
+        int bad = 0;
+        int64_t pred = (t == 0) ? last_verified[b] : cand_idx[(b * L + t - 1) * K + i];
+        pred = clamp_id(pred, V, &bad);
+        for (int64_t j = 0; j < K; ++j) {
+          int64_t cur = clamp_id(cand_idx[(b * L + t) * K + j], V, &bad);
+          double acc = 0.0;
+          for (int64_t q = 0; q < r; ++q)
+            acc += widen_bf16(A[pred * r + q]) * Ht[q] * widen_bf16(Bt[cur * r + q]);
+          S[((b * L + t) * K + i) * K + j] = static_cast<double>(cand_val[(b * L + t) * K + j]) + acc;
+        }
+        any_bad |= bad;
+      }
+    }
+  }
+  return any_bad;
+}
+
+// ---------------------------------------------------------------------------
+// Stage 3: the walk over precomputed scores, "A Lightweight Path Selector":
+// starting from the last verified token, greedy follows the best successor at
+// each step; sampling draws from the same scores.
+//   row(t) = 0 for t = 0 (all rows are equal there), else slot(t - 1).
+//   temperature <= 0: slot(t) = lowest j maximising S[b, t, row, j] (R4);
+//                     q[b, t, :] = one-hot at slot(t).
+//   temperature  > 0: w_j = exp((S_j - max S) / T) in double, Z = w_0 + ... + w_15
+//                     summed in slot order, u = uniform24(seed, b, t, 0, offset),
+//                     slot(t) = smallest j with u * Z < w_0 + ... + w_j (R5);
+//                     q[b, t, j] = w_j / Z.
+// S: [B, L, K, K] fp32 (the walk reads scores at the precision they are stored);
+// outputs draft_tok, draft_slot: [B, L]; q: [B, L, K] or null;
+// margin: [B] or null -- per sequence the smallest decision margin met on the
+// path (greedy: best - runner-up; sampled: distance of u*Z to the nearest CDF
+// boundary of the chosen slot, relative to Z).
+// ---------------------------------------------------------------------------
+void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int64_t K,
+                 double temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
+                 int32_t* draft_slot, float* q, double* margin, int nthreads) {
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t prev = 0;
+    double min_margin = std::numeric_limits<double>::infinity();
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t row = (t == 0) ? 0 : prev;
+      const float* s = S + ((b * L + t) * K + row) * K;
+      int64_t best = 0;
+      for (int64_t j = 1; j < K; ++j)
+        if (s[j] > s[best]) best = j;
+      int64_t chosen;
+      if (temperature <= 0.0) {
+        chosen = best;
+        double runner = -std::numeric_limits<double>::infinity();
+        for (int64_t j = 0; j < K; ++j)
+          if (j != best) runner = std::max(runner, static_cast<double>(s[j]));
+        min_margin = std::min(min_margin, static_cast<double>(s[best]) - runner);
+        if (q)
+          for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = (j == chosen) ? 1.0f : 0.0f;
+      } else {
+        const double m = static_cast<double>(s[best]);
+        std::vector<double> w(static_cast<size_t>(K)), cdf(static_cast<size_t>(K));
+        double Z = 0.0;
+        for (int64_t j = 0; j < K; ++j) {
+          w[j] = std::exp((static_cast<double>(s[j]) - m) / temperature);
+          Z += w[j];
+          cdf[j] = Z;
+        }
+        const double u = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 0, offset);
+        const double target = u * Z;
+        chosen = -1;
+        for (int64_t j = 0; j < K; ++j)
+          if (target < cdf[j]) {
+            chosen = j;
+            break;
+          }
+        if (chosen < 0)
+          for (int64_t j = K - 1; j >= 0; --j)
+            if (w[j] > 0.0) {
+              chosen = j;
+              break;
+            }
+        double gap = cdf[chosen] - target;
+        if (chosen > 0) gap = std::min(gap, target - cdf[chosen - 1]);
+        min_margin = std::min(min_margin, gap / Z);
+        if (q)
+          for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = static_cast<float>(w[j] / Z);
+      }
+      draft_slot[b * L + t] = static_cast<int32_t>(chosen);
+      draft_tok[b * L + t] = cand_idx[(b * L + t) * K + chosen];
+      prev = chosen;
+    }
+    if (margin) margin[b] = min_margin;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 4: two-tap dynamic depthwise convolution, "A Lightweight Local
+// Convolution": Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}, each
+// coefficient = learned base + a correction from the current hidden state,
+// shared by every 16 channels; position 0 reads the last verified token's
+// representation (reading R6):
+//   c[m, n]  = sum_k W_c[n, k] h[m, k] (+ b_c[n]),   n in [0, 2G), G = d / 16
+//   y[m, ch] = (k0[ch] + c[m, g]) x[m, ch] + (k1[ch] + c[m, G + g]) xp[ch]
+// with g = ch / 16, m = b * L + t, and xp = x[m - 1] for t > 0, x_prev[b] at t = 0.
+// x: [B, L, d]; x_prev: [B, d]; h: [B, L, d] or null (then h = x); k0, k1: [d];
+// W_c: [2G, d] bf16; b_c: [2G] fp32 or null; y: [B, L, d] double.
+// ---------------------------------------------------------------------------
+void oracle_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* h,
+                     const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
+                     const float* b_c, int64_t B, int64_t L, int64_t d, double* y,
+                     int nthreads) {
+  const int64_t G = d / 16;
+  if (!h) h = x;
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
+  for (int64_t m = 0; m < B * L; ++m) {
+    const int64_t b = m / L, t = m % L;
+    std::vector<double> c(static_cast<size_t>(2 * G));
+    for (int64_t n = 0; n < 2 * G; ++n) {
+      double acc = b_c ? static_cast<double>(b_c[n]) : 0.0;
+      for (int64_t kk = 0; kk < d; ++kk) acc += widen_bf16(W_c[n * d + kk]) * widen_bf16(h[m * d + kk]);
+      c[n] = acc;
+    }
+    const uint16_t* xp = (t > 0) ? x + (m - 1) * d : x_prev + b * d;
+    for (int64_t ch = 0; ch < d; ++ch) {
+      const int64_t g = ch / 16;
+      y[m * d + ch] = (widen_bf16(k0[ch]) + c[g]) * widen_bf16(x[m * d + ch]) +
+                      (widen_bf16(k1[ch]) + c[G + g]) * widen_bf16(xp[ch]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 5: block verification against the target's logits.  "A Lightweight
+// Path Selector" (rejection sampling restores the exact target distribution),
+// Table 1's note (the acceptance length includes the verifier's next token),
+// and the post's opening (the target verifies the whole block in one pass).
+//
+// temperature <= 0 (greedy): a_t = lowest id maximising target[b, t, :]
+//   (values compared exactly); n = first t < L with draft_tok[b, t] != a_t,
+//   else L; out = draft[0..n-1], a_n; accept_len = n + 1.
+// temperature > 0 (reading R7): for t = 0..L-1 with p_t = softmax(target_t / T)
+//   (double), x = draft_tok[t], q = draft_q[t, draft_slot[t]],
+//   u = uniform24(seed, b, t, 1, offset): accept iff u * q < p_t(x).
+//   On the first rejection at t: draw from the residual r_v = max(0, p_t(v) - q_t(v))
+//   (q_t(v) = draft_q[t, j] where cand_idx[t, j] = v, else 0) by inverse CDF
+//   in id order with u' = uniform24(seed, b, t, 2, offset); accept_len = t + 1.
+//   If all L are accepted: draw the bonus token from p_L the same way with
+//   uniform24(seed, b, L, 2, offset); accept_len = L + 1.
+// target: [B, L + 1, ld] bf16 (row (b, t) starts at (b * (L + 1) + t) * ld);
+// out_tok: [B, L + 1], -1 after the last emitted token.
+// margin: [B] or null -- the smallest relative decision margin met on the path
+// (T > 0 only; +inf at T = 0, whose decisions are exact).
+// ---------------------------------------------------------------------------
+void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
+                   const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
+                   int64_t B, int64_t L, int64_t K, int64_t V, double temperature,
+                   uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* out_tok,
+                   double* margin, int nthreads) {
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads_for(nthreads))
+  for (int64_t b = 0; b < B; ++b) {
+    int32_t* out = out_tok + b * (L + 1);
+    for (int64_t t = 0; t <= L; ++t) out[t] = -1;
+    double min_margin = std::numeric_limits<double>::infinity();
+    int64_t n = L;
+    int32_t last = -1;
+    if (temperature <= 0.0) {
+      for (int64_t t = 0; t <= L; ++t) {
+        const uint16_t* row = target + (b * (L + 1) + t) * ld;
+        int64_t a = 0;
+        for (int64_t v = 1; v < V; ++v)
+          if (ranks_before(widen_bf16(row[v]), v, widen_bf16(row[a]), a)) a = v;
+        if (t == L || draft_tok[b * L + t] != a) {
+          n = t;
+          last = static_cast<int32_t>(a);
+          break;
+        }
+      }
+    } else {
+      std::vector<double> p(static_cast<size_t>(V));
+      auto softmax_row = [&](int64_t t) {
+        const uint16_t* row = target + (b * (L + 1) + t) * ld;
+        double m = -std::numeric_limits<double>::infinity();
+        for (int64_t v = 0; v < V; ++v) m = std::max(m, widen_bf16(row[v]));
+        double Z = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+          p[v] = std::exp((widen_bf16(row[v]) - m) / temperature);
+          Z += p[v];
+        }
+        for (int64_t v = 0; v < V; ++v) p[v] /= Z;
+      };
+      // Inverse CDF over weights w[0..V) in id order; records the margin.
+      auto draw = [&](const std::vector<double>& w, double u) -> int32_t {
+        double total = 0.0;
+        for (int64_t v = 0; v < V; ++v) total += w[v];
+        const double target_mass = u * total;
+        double run = 0.0, prev_run = 0.0;
+        int64_t chosen = -1;
+        for (int64_t v = 0; v < V; ++v) {
+          prev_run = run;
+          run += w[v];
+          if (target_mass < run) {
+            chosen = v;
+            break;
+          }
+        }
+        if (chosen < 0) {
+          for (int64_t v = V - 1; v >= 0; --v)
+            if (w[v] > 0.0) {
+              chosen = v;
+              break;
+            }
+          prev_run = run;
+        }
+        double gap = std::min(run - target_mass, target_mass - prev_run);
+        min_margin = std::min(min_margin, gap / total);
+        return static_cast<int32_t>(chosen);
+      };
+      n = L;
+      for (int64_t t = 0; t < L; ++t) {
+        softmax_row(t);
+        const int32_t x = draft_tok[b * L + t];
+        const double qx = static_cast<double>(draft_q[(b * L + t) * K + draft_slot[b * L + t]]);
+        const double px = (x >= 0 && x < V) ? p[x] : 0.0;
+        const double u = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 1, offset);
+        const double lhs = u * qx;
+        min_margin = std::min(min_margin, std::fabs(lhs - px) / std::max(px, 1e-300));
+        if (lhs < px) continue;
+        std::vector<double> resid(p);
+        for (int64_t j = 0; j < K; ++j) {
+          const int32_t v = cand_idx[(b * L + t) * K + j];
+          if (v >= 0 && v < V)
+            resid[v] = std::max(0.0, p[v] - static_cast<double>(draft_q[(b * L + t) * K + j]));
+        }
+        n = t;
+        last = draw(resid, uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 2, offset));
+        break;
+      }
+      if (n == L) {
+        softmax_row(L);
+        last = draw(p, uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(L), 2, offset));
+      }
+    }
+    for (int64_t t = 0; t < n; ++t) out[t] = draft_tok[b * L + t];
+    out[n] = last;
+    accept_len[b] = static_cast<int32_t>(n + 1);
+    if (margin) margin[b] = min_margin;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused LM head + top-k, restated unfused: logits[m, v] = sum_k hidden[m, k] W[v, k]
+// in double for the requested rows only, then the top-k of each row by
+// reading R1 (the head produces U_t, "DFlash's own logit", "A Lightweight Path
+// Selector").  hidden: [M, d] bf16; W: [V, d] bf16; rows: [n_rows] row ids;
+// vals (double) / idx: [n_rows, k].
+// ---------------------------------------------------------------------------
+void oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t V, int64_t d,
+                        const int64_t* rows, int64_t n_rows, int k, double* vals,
+                        int32_t* idx, int nthreads) {
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads_for(nthreads))
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const uint16_t* hrow = hidden + rows[i] * d;
+    std::vector<double> logit(static_cast<size_t>(V));
+    for (int64_t v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int64_t kk = 0; kk < d; ++kk) acc += widen_bf16(hrow[kk]) * widen_bf16(W[v * d + kk]);
+      logit[v] = acc;
+    }
+    std::vector<int64_t> order(static_cast<size_t>(V));
+    for (int64_t v = 0; v < V; ++v) order[v] = v;
+    std::partial_sort(order.begin(), order.begin() + k, order.end(),
+                      [&logit](int64_t a, int64_t b) { return ranks_before(logit[a], a, logit[b], b); });
+    for (int j = 0; j < k; ++j) {
+      vals[i * k + j] = logit[order[j]];
+      idx[i * k + j] = static_cast<int32_t>(order[j]);
+    }
+  }
+}
+
+// The thread count an OpenMP region would use for `nthreads` (reported as the
+// CPU baseline's core count).
+int oracle_threads(int nthreads) {
+#ifdef _OPENMP
+  int used = 1;
+#pragma omp parallel num_threads(threads_for(nthreads))
+  {
+#pragma omp single
+    used = omp_get_num_threads();
+  }
+  return used;
+#else
+  (void)nthreads;
+  return 1;
+#endif
+}
+
+}  // extern "C"
