@@ -1,0 +1,504 @@
+"""Benchmark of the DFlash 2 draft-block head on GB300.
+
+One step = one full draft-verify cycle of the head over a batch of sequences
+(the whole hot path): two-tap dynamic conv x10 (each application on its own
+activation, the last one feeding the gate) -> top-16 -> context gate + pair
+scores -> walk (T=0) -> verify (T=0) -> walk (T=1) -> verify (T=1), on seeded
+synthetic inputs of the pages' shapes (B=128, L=16, V=151936, d=5120).
+
+Prints ONE JSON line (rank 0).  `value` is draft blocks per second with the
+inputs resident in HBM; `e2e` is the same metric through the public API with
+host (pinned) buffers, host<->device copies inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dflash2|reference]
+                  [--no-sweep] [--no-e2e] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from draft_selection_dflash2_gb300 import synth  # noqa: E402
+
+METRIC = "draft blocks/s"
+UNIT = "blocks/s"
+B, L, V, D, R, K = 128, 16, 151936, 5120, 256, 16
+CONV_APPS = 10
+WORKLOAD = (f"full draft-verify cycle B={B} L={L} V={V} d={D}: two-tap conv x{CONV_APPS} (each on its own "
+            "[B,L,d] activation), top-16, gate + pair scores, walk T=0 and T=1, verify T=0 and T=1")
+PAIRS_PER_BLOCK = K + K * K * (L - 1)   # 16 at t=0 (one predecessor), 256 per later position
+SWEEP_B = (1, 8, 32, 128, 256)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per stage (what the method must move, not what a kernel does)
+# ---------------------------------------------------------------------------
+def bytes_topk(nb):
+    return nb * L * V * 2 + nb * L * K * 8
+
+
+def bytes_pairs(nb):
+    per_block = L * D * 2 + (K * (L - 1) + 1) * R * 2 + K * L * R * 2 + L * K * K * 4 + L * K * 8
+    return nb * per_block + R * D * 2
+
+
+def bytes_conv(nb):
+    return nb * L * D * 2 * 2 + nb * D * 2 + 2 * (D // 16) * D * 2 + 2 * D * 2
+
+
+def bytes_verify(acc):
+    return int(np.sum(acc.astype(np.int64))) * V * 2
+
+
+def bytes_walk(nb):
+    return nb * L * K * K * 4 + nb * L * K * 4
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled with nvidia-smi during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, torch):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dflash2_clocks_{os.getpid()}.csv")
+        try:
+            p = torch.cuda.get_device_properties(torch.cuda.current_device())
+            self.sel = ["-i", f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 6:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[2:6]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def make_host_workload(nb, sweep_rows=0):
+    """Seeded host tensors of the full-cycle workload (bf16 as uint16 bits)."""
+    rng = np.random.default_rng(0)
+    rows = max(nb * L, sweep_rows)
+    w = {}
+    w["U"] = synth.logits_planted(rng, rows, V)
+    # each conv application reads its own activation (in the drafter every
+    # sublayer boundary presents a new hidden state), so nothing is chained
+    w["conv"] = [(synth.normal_bits(100 + a, (nb, L, D)), synth.normal_bits(200 + a, (nb, D)))
+                 + synth.conv_layer_params(10 + a, D) for a in range(CONV_APPS)]
+    w["W_H"] = synth.normal_bits(3, (R, D), std=0.02)
+    w["A"] = synth.normal_bits(4, (V, R), std=0.02)
+    w["Bt"] = synth.normal_bits(5, (V, R), std=0.02)
+    w["last_verified"] = np.random.default_rng(6).integers(0, V, nb).astype(np.int32)
+    return w
+
+
+def to_dev(torch, a, dev):
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a))
+    t = t.to(dev)
+    return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+
+class Cycle:
+    """Device buffers and the step of the full cycle, through the Python API."""
+
+    def __init__(self, torch, api, h, w, nb, dev):
+        self.torch, self.api, self.h, self.nb = torch, api, h, nb
+        bf = lambda a: to_dev(torch, a, dev)  # noqa: E731
+        self.U = bf(w["U"][: nb * L])
+        self.conv = [(bf(x), bf(xp), bf(k0), bf(k1), bf(W)) for x, xp, k0, k1, W in w["conv"]]
+        self.W_H, self.A, self.Bt = bf(w["W_H"]), bf(w["A"]), bf(w["Bt"])
+        self.lv = to_dev(torch, w["last_verified"], dev)
+        self.ybuf = [torch.empty((nb, L, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.vals = torch.empty((nb * L, K), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((nb * L, K), dtype=torch.int32, device=dev)
+        self.gate = torch.empty((nb, L, R), dtype=torch.float32, device=dev)
+        self.S = torch.empty((nb, L, K, K), dtype=torch.float32, device=dev)
+        self.tok = [torch.empty((nb, L), dtype=torch.int32, device=dev) for _ in range(2)]
+        self.slot = [torch.empty((nb, L), dtype=torch.int32, device=dev) for _ in range(2)]
+        self.q = [torch.empty((nb, L, K), dtype=torch.float32, device=dev) for _ in range(2)]
+        self.acc = [torch.empty((nb,), dtype=torch.int32, device=dev) for _ in range(2)]
+        self.out = [torch.empty((nb, L + 1), dtype=torch.int32, device=dev) for _ in range(2)]
+        self.target = None
+        self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 3)
+
+    def step(self, ev=None, seed_offset=0):
+        api, h = self.api, self.h
+        rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
+        rec("start")
+        for a, (x, xp, k0, k1, W) in enumerate(self.conv):
+            cur = api.conv2tap(h, x, xp, k0, k1, W, y=self.ybuf[a % 2])
+        rec("conv")
+        api.topk(h, self.U, vals=self.vals, idx=self.idx)
+        rec("topk")
+        ci, cv = self.idx.view(self.nb, L, K), self.vals.view(self.nb, L, K)
+        api.pair_scores(h, ci, cv, self.lv, cur, self.W_H, None, self.A, self.Bt, gate=self.gate, S=self.S)
+        rec("pairs")
+        for i, T in enumerate((0.0, 1.0)):
+            api.walk(h, self.S, ci, temperature=T, seed=1, offset=seed_offset, draft_tok=self.tok[i],
+                     draft_slot=self.slot[i], draft_q=self.q[i])
+            rec(f"walk{i}")
+            api.verify(h, self.target, self.tok[i], self.slot[i], self.q[i], ci, temperature=T, seed=1,
+                       offset=seed_offset, accept_len=self.acc[i], out_tok=self.out[i])
+            rec(f"verify{i}")
+
+
+STAGES = ["conv", "topk", "pairs", "walk0", "verify0", "walk1", "verify1"]
+
+
+def run_gpu(args):
+    import torch
+
+    from draft_selection_dflash2_gb300 import api, build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        build.build()
+    if dist:
+        dist.barrier()
+    build.build()
+    pk = peaks()
+    h = api.Handle(torch.cuda.current_device())
+
+    sweep_rows = max(SWEEP_B) * L if (args.sweep and rank == 0) else 0
+    w = make_host_workload(B, sweep_rows)
+    cyc = Cycle(torch, api, h, w, B, dev)
+    # plant the target on the greedy draft of one untimed cycle: 0.85 argmax agreement
+    cyc.target = torch.empty((B, L + 1, V), dtype=torch.bfloat16, device=dev)
+    cyc.step()
+    torch.cuda.synchronize()
+    draft = cyc.tok[0].cpu().numpy()
+    tgt = synth.target_planted(7, draft, V, agree=0.85, plant=8.0)
+    cyc.target.copy_(to_dev(torch, tgt, dev))
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        cyc.step(seed_offset=i)
+    torch.cuda.synchronize()
+    assert h.device_error() == 0, "device error during warm-up"
+
+    # timed region
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in ["start"] + STAGES} for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(args.steps):
+        cyc.step(ev=evs[i], seed_offset=1000 + i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    assert h.device_error() == 0, "device error during the timed region"
+
+    stage_ms = {}
+    for n in STAGES:
+        prev = ["start"] + STAGES
+        p = prev[prev.index(n) - 1]
+        stage_ms[n] = statistics.median(evs[i][p].elapsed_time(evs[i][n]) for i in range(args.steps))
+    acc0 = cyc.acc[0].cpu().numpy()
+    acc1 = cyc.acc[1].cpu().numpy()
+
+    value = world * B * args.steps / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+    hbm = pk["hbm_gbs"]
+    stage_bytes = {"conv": CONV_APPS * bytes_conv(B), "topk": bytes_topk(B), "pairs": bytes_pairs(B),
+                   "walk0": bytes_walk(B), "verify0": bytes_verify(acc0), "walk1": bytes_walk(B),
+                   "verify1": bytes_verify(acc1)}
+    stages = {}
+    for n in STAGES:
+        gbs = stage_bytes[n] / (stage_ms[n] * 1e-3) / 1e9
+        stages[n] = {"ms": round(stage_ms[n], 4), "alg_bytes": stage_bytes[n], "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / hbm, 4)}
+    stages["conv"]["per_application_ms"] = round(stage_ms["conv"] / CONV_APPS, 4)
+    dom = max(STAGES, key=lambda n: stage_ms[n])
+    kernel_name = {"conv": "conv2tap_kernel", "topk": "topk16_kernel", "pairs": "gate_kernel + pair_kernel",
+                   "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_rows_kernel",
+                   "verify1": "verify_rows_kernel"}[dom]
+    per_launch_ms = stage_ms[dom] / (CONV_APPS if dom == "conv" else 1)
+    per_launch_bytes = stage_bytes[dom] / (CONV_APPS if dom == "conv" else 1)
+    achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kernel_name, "stage": dom, "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak_source": pk["source"] + " (burst copy, MEASURED_PEAKS.json)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate (fp64 sampling decisions)",
+        "data": "synthetic (seeded; shapes of the pages' workloads, no datasets or trained weights)",
+        "config": {"workload": WORKLOAD, "B": B, "L": L, "V": V, "d": D, "K": K, "r": R,
+                   "conv_applications": CONV_APPS, "parallelism": f"replicas x{world} (batch-sharded)",
+                   "l2": "inputs larger than L2 (622 MB logits + 661 MB target logits per step)"},
+        "pair_scores_per_s": round(B * PAIRS_PER_BLOCK / (stage_ms["pairs"] * 1e-3), 1),
+        "mean_accept_len": {"T0": round(float(acc0.mean()), 4), "T1": round(float(acc1.mean()), 4)},
+        "stages": stages,
+        "roofline": roofline,
+        "clocks": clk,
+        "gpu_launches": cyc.launches_per_step * args.steps,
+    }
+
+    if rank == 0 and args.sweep:
+        line["sweep"] = run_sweep(torch, api, h, w, cyc, dev, pk)
+    if rank == 0 and args.e2e:
+        line["e2e"] = run_e2e(torch, api, h, w, cyc, dev, args)
+    if rank == 0 and args.cpu_baseline and world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=8)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_sweep(torch, api, h, w, cyc, dev, pk):
+    """Batch sweep at d=5120: top-16 + pair scores + greedy walk, blocks/s and GB/s per stage."""
+    out = []
+    Ufull = to_dev(torch, w["U"][: max(SWEEP_B) * L], dev)
+    hs_all = torch.empty((max(SWEEP_B), L, D), dtype=torch.bfloat16, device=dev)
+    hs_all.copy_(cyc.ybuf[1][:1].expand(max(SWEEP_B), L, D))
+    lv = torch.zeros((max(SWEEP_B),), dtype=torch.int32, device=dev)
+    for nb in SWEEP_B:
+        U = Ufull[: nb * L]
+        vals = torch.empty((nb * L, K), dtype=torch.float32, device=dev)
+        idx = torch.empty((nb * L, K), dtype=torch.int32, device=dev)
+        gate = torch.empty((nb, L, R), dtype=torch.float32, device=dev)
+        S = torch.empty((nb, L, K, K), dtype=torch.float32, device=dev)
+        tok = torch.empty((nb, L), dtype=torch.int32, device=dev)
+        slot = torch.empty((nb, L), dtype=torch.int32, device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        times = {"topk": [], "pairs": [], "walk": []}
+        steps = 20
+        for it in range(steps + 3):
+            flush.zero_()   # L2 flush (buffer larger than L2)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+            api.topk(h, U, vals=vals, idx=idx)
+            e[1].record()
+            api.pair_scores(h, idx.view(nb, L, K), vals.view(nb, L, K), lv[:nb], hs_all[:nb], cyc.W_H, None,
+                            cyc.A, cyc.Bt, gate=gate, S=S)
+            e[2].record()
+            api.walk(h, S, idx.view(nb, L, K), draft_tok=tok, draft_slot=slot, want_q=False)
+            e[3].record()
+            torch.cuda.synchronize()
+            if it >= 3:
+                times["topk"].append(e[0].elapsed_time(e[1]))
+                times["pairs"].append(e[1].elapsed_time(e[2]))
+                times["walk"].append(e[2].elapsed_time(e[3]))
+        del flush
+        med = {k: statistics.median(v) for k, v in times.items()}
+        tot = sum(med.values())
+        out.append({"B": nb, "blocks_per_s": round(nb / (tot * 1e-3), 1), "ms": round(tot, 4),
+                    "pair_scores_per_s": round(nb * PAIRS_PER_BLOCK / (med["pairs"] * 1e-3), 1),
+                    "topk_GBps": round(bytes_topk(nb) / (med["topk"] * 1e-3) / 1e9, 1),
+                    "pairs_GBps": round(bytes_pairs(nb) / (med["pairs"] * 1e-3) / 1e9, 1),
+                    "topk_frac_hbm": round(bytes_topk(nb) / (med["topk"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                    "walk_us": round(med["walk"] * 1e3, 2)})
+    return out
+
+
+def run_e2e(torch, api, h, w, cyc, dev, args):
+    """Same cycle through the public API from pinned host buffers: H2D of the
+    step's inputs (activations, drafter logits, target logits, last verified
+    tokens) and D2H of the acceptance lengths and emitted tokens, timed."""
+    host = {
+        "U": torch.from_numpy(w["U"][: B * L].view(np.int16)).pin_memory(),
+        "target": cyc.target.view(torch.int16).cpu().pin_memory(),
+        "lv": torch.from_numpy(w["last_verified"]).pin_memory(),
+    }
+    for a, (x, xp, *_rest) in enumerate(w["conv"]):
+        host[f"x{a}"] = torch.from_numpy(x.view(np.int16)).pin_memory()
+        host[f"xp{a}"] = torch.from_numpy(xp.view(np.int16)).pin_memory()
+    res = {"acc": [torch.empty((B,), dtype=torch.int32).pin_memory() for _ in range(2)],
+           "out": [torch.empty((B, L + 1), dtype=torch.int32).pin_memory() for _ in range(2)]}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for v in res.values() for t in v)
+    dst = {"U": cyc.U.view(torch.int16), "target": cyc.target.view(torch.int16), "lv": cyc.lv}
+    for a, (x, xp, *_rest) in enumerate(cyc.conv):
+        dst[f"x{a}"] = x.view(torch.int16)
+        dst[f"xp{a}"] = xp.view(torch.int16)
+
+    def step(i):
+        for k in host:
+            dst[k].copy_(host[k], non_blocking=True)
+        cyc.step(seed_offset=2000 + i)
+        for j in range(2):
+            res["acc"][j].copy_(cyc.acc[j], non_blocking=True)
+            res["out"][j].copy_(cyc.out[j], non_blocking=True)
+
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, args.steps // 2)
+    t0.record()
+    for i in range(n):
+        step(i)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    return {"value": round(B * n / (ms * 1e-3), 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 4)}
+
+
+def oracle_cycle(w, target_bits, nb, nthreads):
+    """The oracle's own chain on the first nb sequences of the workload."""
+    import oracle
+    for x, xp, k0, k1, W in w["conv"]:
+        cur = synth.bf16_bits(oracle.conv2tap(x[:nb], xp[:nb], k0, k1, W, nthreads=nthreads).astype(np.float32))
+    ov, oi = oracle.topk(w["U"][: nb * L], nthreads=nthreads)
+    ci, cv = oi.reshape(nb, L, K), ov.reshape(nb, L, K)
+    H = oracle.gate(cur.reshape(nb * L, D), w["W_H"], None, nthreads=nthreads).reshape(nb, L, R)
+    S, _ = oracle.pair_scores(ci, cv, w["last_verified"][:nb], H, w["A"], w["Bt"], nthreads=nthreads)
+    S32 = S.astype(np.float32)
+    accs = []
+    for T in (0.0, 1.0):
+        tok, slot, q, _ = oracle.walk(S32, ci, temperature=T, seed=1, nthreads=nthreads)
+        acc, _, _ = oracle.verify(target_bits[:nb], tok, slot, q, ci, temperature=T, seed=1, nthreads=nthreads)
+        accs.append(acc)
+    return accs
+
+
+def run_cpu_baseline(w, cyc, target_bits, sample=8):
+    import oracle
+    threads = oracle.default_threads()
+    used = oracle.threads_used(threads)
+    t = time.perf_counter()
+    oracle_cycle(w, target_bits, sample, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(sample / dt, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"first {sample} of {B} sequences of the workload, one full cycle ({dt:.1f} s)"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one full cycle over a
+    bounded sample of the workload's sequences, on all host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    sample = 4
+    w = make_host_workload(sample)
+    rng_tok = np.random.default_rng(7).integers(0, V, (sample, L)).astype(np.int32)
+    target = synth.target_planted(7, rng_tok, V, agree=0.85, plant=8.0)
+    threads = oracle.default_threads()
+    used = oracle.threads_used(threads)
+    for _ in range(args.warmup):
+        oracle_cycle(w, target, sample, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_cycle(w, target, sample, threads)
+    dt = time.perf_counter() - t
+    value = sample * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD, "B": B, "L": L, "V": V, "d": D,
+                       "sample_sequences_per_step": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"{sample} of {B} sequences per step, full cycle"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dflash2", choices=["dflash2", "reference"])
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,115 @@
+// walk.cu -- the walk over precomputed pair scores ("DFlash 2: Keep Drafting
+// Parallel", "A Lightweight Path Selector": starting from the last verified
+// token, greedy follows the best successor at each step; sampling draws from
+// the same scores).  This is the only sequential part of the draft-block head.
+//
+// One warp per sequence.  The warp first copies the sequence's whole score
+// block S[b] ([L, 16, 16] fp32, 1 KB per position) into shared memory with
+// 16-byte loads, so the L dependent steps run out of shared memory instead of
+// paying a global-memory round trip each.  Lane j (j < 16) owns successor slot j.
+//   greedy : shuffle arg-max over (value, lowest slot).
+//   sampled: w_j = exp((S_j - max) / T) in fp64; lane 0 sums Z and the CDF in
+//            slot order and draws with the Philox uniform of (b, t, stream 0).
+#include "common.cuh"
+#include "launch.h"
+#include "philox.cuh"
+
+namespace dflash2 {
+namespace {
+
+constexpr int kWalkWarps = 2;            // sequences per CTA (2 x 64 KB at L = 64)
+constexpr int kMaxWalkL = 64;
+
+__global__ void __launch_bounds__(kWalkWarps * 32)
+    walk_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand_idx, int64_t B,
+                int64_t L, double temperature, uint64_t seed, uint64_t offset,
+                int32_t* __restrict__ draft_tok, int32_t* __restrict__ draft_slot,
+                float* __restrict__ draft_q) {
+  extern __shared__ __align__(16) float wsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * kWalkWarps + warp;
+  if (b >= B) return;
+  float* sb = wsm + static_cast<size_t>(warp) * L * kTopK * kTopK;
+  const float4* src = reinterpret_cast<const float4*>(S + b * L * kTopK * kTopK);
+  float4* dst = reinterpret_cast<float4*>(sb);
+  const int n4 = static_cast<int>(L * kTopK * kTopK / 4);
+  for (int i = lane; i < n4; i += 32) dst[i] = src[i];
+  __syncwarp();
+
+  const int j = lane & (kTopK - 1);
+  int prev = 0;
+  for (int64_t t = 0; t < L; ++t) {
+    const float v = sb[(t * kTopK + prev) * kTopK + j];
+    // arg-max with the lowest slot on ties (lanes 16..31 mirror 0..15)
+    float bv = v;
+    int bj = j;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, o);
+      if (ov > bv || (ov == bv && oj < bj)) {
+        bv = ov;
+        bj = oj;
+      }
+    }
+    int chosen;
+    const int64_t q_at = (b * L + t) * kTopK + j;
+    if (temperature <= 0.0) {
+      chosen = bj;
+      if (draft_q && lane < kTopK) draft_q[q_at] = (j == chosen) ? 1.0f : 0.0f;
+    } else {
+      const double w = exp((static_cast<double>(v) - static_cast<double>(bv)) / temperature);
+      // Every lane gathers the 16 weights and repeats the (identical) slot-order
+      // sums, so no broadcast is needed afterwards.
+      double wj[kTopK];
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i) wj[i] = __shfl_sync(0xFFFFFFFFu, w, i);
+      double Z = 0.0;
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i) Z += wj[i];
+      const double target =
+          philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset) * Z;
+      int pick = -1;
+      double run = 0.0;
+#pragma unroll
+      for (int i = 0; i < kTopK; ++i) {
+        run += wj[i];
+        if (pick < 0 && target < run) pick = i;
+      }
+      if (pick < 0)
+        for (int i = kTopK - 1; i >= 0; --i)
+          if (wj[i] > 0.0) {
+            pick = i;
+            break;
+          }
+      chosen = pick;
+      if (draft_q && lane < kTopK) draft_q[q_at] = static_cast<float>(w / Z);
+    }
+    if (lane == 0) {
+      draft_slot[b * L + t] = chosen;
+      draft_tok[b * L + t] = cand_idx[(b * L + t) * kTopK + chosen];
+    }
+    prev = chosen;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
+                        float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
+                        int32_t* draft_slot, float* draft_q, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(kWalkWarps) * L * kTopK * kTopK * sizeof(float);
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kWalkWarps * kMaxWalkL * kTopK * kTopK * 4);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>((B + kWalkWarps - 1) / kWalkWarps);
+  walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, static_cast<double>(temperature),
+                                                       seed, offset, draft_tok, draft_slot, draft_q);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash2

@@ -1,0 +1,207 @@
+/*
+ * dflash2.h -- C ABI of the DFlash 2 draft-block head for NVIDIA GB300 (sm_103a).
+ *
+ * The draft-block head turns a parallel drafter's per-position outputs into one
+ * coherent draft block and verifies it ("DFlash 2: Keep Drafting Parallel",
+ * Inco AI):
+ *   dflash2_topk          top-16 candidates per block position
+ *   dflash2_pair_scores   context gate + pairwise path-selector scores
+ *   dflash2_walk          greedy or temperature-sampled walk over the scores
+ *   dflash2_conv2tap      two-tap dynamic depthwise convolution
+ *   dflash2_verify        block verification -> acceptance lengths
+ *   dflash2_lmhead_topk   LM head GEMM with a streaming top-16 epilogue
+ *
+ * Conventions for every call
+ *   - Pointers marked "device" are CUDA device pointers on the handle's device;
+ *     "host" pointers are ordinary host memory.  The caller owns every buffer:
+ *     the library never frees a pointer or keeps one past the call, and no call
+ *     on the compute path allocates memory.
+ *   - bf16 tensors are passed as `const uint16_t*` holding bf16 bit patterns.
+ *   - Tensors are row-major and contiguous unless an explicit leading dimension
+ *     (`ld`, in elements) is given.  bf16 base pointers must be 16-byte aligned
+ *     and `ld` a multiple of 8; fp32/int32 pointers 4-byte aligned.
+ *   - Token ids are int32; V must be < 2^31.  K (candidates per position) is 16.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Outputs are valid once the stream reaches the call.
+ *   - The return value is a dflash2_status.  Argument errors are detected on
+ *     the host before anything is launched and leave outputs untouched.  No C++
+ *     exception crosses this ABI.
+ *   - Data-dependent errors found on the device (an out-of-range token id, a
+ *     bounded wait that gave up) never fault: the kernel clamps the access,
+ *     ORs a DFLASH2_DEVERR_* bit into the handle's device error word and
+ *     continues; read it with dflash2_get_device_error().
+ *   - A handle may be used from one host thread at a time.  Calls that share a
+ *     handle but run on different streams only share the error word.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dflash2_handle dflash2_handle;
+
+enum dflash2_status {
+  DFLASH2_OK = 0,
+  DFLASH2_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent size      */
+  DFLASH2_ERR_UNSUPPORTED = -2, /* k != 16, V < 16, d % 16 != 0, L > 64, ...         */
+  DFLASH2_ERR_MISALIGNED = -3,  /* a pointer or leading dimension breaks alignment  */
+  DFLASH2_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed      */
+  DFLASH2_ERR_TIMEOUT = -5,     /* a bounded device wait gave up (see error word)   */
+  DFLASH2_ERR_DEVICE = -6,      /* the device error word is non-zero                */
+  DFLASH2_ERR_WORKSPACE = -7    /* the caller's workspace is too small              */
+};
+
+/* Bits of the device error word. */
+#define DFLASH2_DEVERR_BAD_TOKEN 0x1u /* a token id outside [0, V) was clamped     */
+#define DFLASH2_DEVERR_TIMEOUT 0x2u   /* a bounded wait (TMA / mbarrier) gave up  */
+#define DFLASH2_DEVERR_BAD_SLOT 0x4u  /* a draft slot outside [0, 16) was clamped */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dflash2_version(void);
+
+/* Human-readable name of a dflash2_status value (static storage). */
+const char* dflash2_status_string(int status);
+
+/*
+ * Creates a handle bound to CUDA device `device`.  Allocates the 4-byte device
+ * error word (the only allocation the library ever makes) and records the SM
+ * count.  Makes `device` current on the calling thread.
+ */
+int dflash2_create(int device, dflash2_handle** out);
+
+/* Frees the handle and its error word.  Synchronises the device first. */
+int dflash2_destroy(dflash2_handle* h);
+
+/* Number of SMs of the handle's device (host). */
+int dflash2_num_sms(const dflash2_handle* h);
+
+/*
+ * Synchronises `stream`, copies the device error word to *bits (host) and, if
+ * `clear` is non-zero, resets it to 0.
+ */
+int dflash2_get_device_error(dflash2_handle* h, void* stream, uint32_t* bits, int clear);
+
+/*
+ * Top-k candidates per row.  "A Lightweight Path Selector": DFlash 2 keeps the
+ * top 16 candidates of the drafter's own logits U_t at every block position.
+ *
+ *   logits  device bf16 [rows, ld]; only columns [0, V) are read.
+ *   vals    device fp32 [rows, k]  -- the candidates' logits (exact bf16 values)
+ *   idx     device int32 [rows, k] -- their vocabulary ids
+ * Order: value descending, ties by lowest id; -0 == +0; NaN ranks below -inf.
+ * k must be 16; 16 <= V < 2^31; ld >= V, ld % 8 == 0; logits 16-byte aligned.
+ * rows == 0 is a no-op.  No workspace: rows with few positions are split over a
+ * thread-block cluster whose partial lists meet in distributed shared memory.
+ */
+int dflash2_topk(dflash2_handle* h, const uint16_t* logits, int64_t rows, int64_t V, int64_t ld,
+                 int k, float* vals, int32_t* idx, void* stream);
+
+/*
+ * Context gate and pairwise path-selector scores.  "A Lightweight Path
+ * Selector", score equation S_t(a,b) = U_t(b) + <A(a) (.) H(h_t), B(b)>:
+ *
+ *   H[b,t,:]   = sigmoid(W_H h[b,t,:] + b_H)                       (r = 256)
+ *   S[b,t,i,j] = cand_val[b,t,j] + sum_q A[p_i,q] H[b,t,q] Bt[cand_idx[b,t,j],q]
+ *   p_i = cand_idx[b,t-1,i] for t >= 1; p_i = last_verified[b] for t = 0, so the
+ *   16 rows of S[b,0] are equal.
+ *
+ *   cand_idx, cand_val  device [B, L, 16] int32 / fp32 (dflash2_topk's output)
+ *   last_verified       device int32 [B]
+ *   hs                  device bf16 [B, L, d] drafter hidden states
+ *   W_H                 device bf16 [256, d];  b_H device fp32 [256] or NULL (= 0)
+ *   A, Bt               device bf16 [V, 256] predecessor / candidate embeddings
+ *   gate                device fp32 [B, L, 256] output: H (also the GEMM result)
+ *   S                   device fp32 [B, L, 16, 16] output
+ * d % 64 == 0, L <= 64.  Ids outside [0, V) are clamped and flagged.
+ */
+int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float* cand_val,
+                        const int32_t* last_verified, const uint16_t* hs, const uint16_t* W_H,
+                        const float* b_H, const uint16_t* A, const uint16_t* Bt, int64_t B,
+                        int64_t L, int64_t d, int64_t V, float* gate, float* S, void* stream);
+
+/*
+ * The walk over precomputed scores.  "A Lightweight Path Selector": from the
+ * last verified token, greedy follows the best successor at each step and
+ * sampling draws from the same scores.  Step t reads row 0 of S[b,0] at t = 0
+ * and row draft_slot[b,t-1] afterwards.
+ *   temperature <= 0: slot = lowest j maximising the row; draft_q one-hot.
+ *   temperature  > 0: w_j = exp((S_j - max S) / T) in fp64, Z summed in slot
+ *     order, u = Philox4x32-10 uniform of counter (b, t | 0 << 24, offset_lo,
+ *     offset_hi), key (seed_lo, seed_hi), u = (x0 >> 8) * 2^-24; slot = smallest j
+ *     with u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.
+ *   S          device fp32 [B, L, 16, 16];  cand_idx device int32 [B, L, 16]
+ *   draft_tok  device int32 [B, L];  draft_slot device int32 [B, L]
+ *   draft_q    device fp32 [B, L, 16] or NULL
+ */
+int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
+                 float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
+                 int32_t* draft_slot, float* draft_q, void* stream);
+
+/*
+ * Two-tap dynamic depthwise convolution.  "A Lightweight Local Convolution":
+ * Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}; each coefficient is a
+ * learned base plus a correction from the current hidden state shared by every
+ * 16 channels; position 0 reads the last verified token's representation.
+ *   [c0; c1][b,t,:] = W_c h[b,t,:] (+ b_c)          W_c: [2d/16, d]
+ *   y[b,t,ch] = (k0[ch] + c0[b,t,ch/16]) x[b,t,ch] + (k1[ch] + c1[b,t,ch/16]) xp[ch]
+ *   xp = x[b,t-1,:] for t > 0, x_prev[b,:] for t = 0.
+ *   x       device bf16 [B, L, d];  x_prev device bf16 [B, d]
+ *   hs      device bf16 [B, L, d] or NULL (then h = x)
+ *   k0, k1  device bf16 [d];  W_c device bf16 [2d/16, d];  b_c device fp32 [2d/16] or NULL
+ *   y       device [B, L, d], fp32 if y_is_fp32 else bf16 (round to nearest even);
+ *           must not overlap x, x_prev or hs.
+ * d % 64 == 0, L <= 64, B <= 65535.
+ */
+int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_prev,
+                     const uint16_t* hs, const uint16_t* k0, const uint16_t* k1,
+                     const uint16_t* W_c, const float* b_c, int64_t B, int64_t L, int64_t d,
+                     void* y, int y_is_fp32, void* stream);
+
+/*
+ * Block verification against the target's logits.  "A Lightweight Path
+ * Selector" (rejection sampling restores the exact target distribution) and
+ * Table 1's note (the acceptance length includes the verifier's next token).
+ *   temperature <= 0: a_t = argmax target[b,t,:] (lowest id on ties);
+ *     n = first t < L with draft_tok[b,t] != a_t (else L);
+ *     out_tok[b] = draft_tok[b,0..n-1], a_n, then -1;  accept_len[b] = n + 1.
+ *   temperature  > 0: speculative rejection sampling with p_t = softmax(target_t/T)
+ *     and q_t = draft_q[b,t,:] on cand_idx[b,t,:] (zero elsewhere): accept t iff
+ *     u1 q_t(x_t) < p_t(x_t); on the first rejection draw from max(0, p_t - q_t)
+ *     by inverse CDF in id order with u2; after L acceptances draw the bonus from
+ *     p_L with u2 at t = L.  u1, u2 are the Philox uniforms of streams 1 and 2.
+ *   target      device bf16 [B, L+1, ld] (row (b,t) at (b*(L+1)+t)*ld)
+ *   draft_tok, draft_slot  device int32 [B, L];  draft_q device fp32 [B, L, 16]
+ *   cand_idx    device int32 [B, L, 16]
+ *   accept_len  device int32 [B];  out_tok device int32 [B, L+1]
+ * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0.
+ */
+int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const int32_t* draft_tok,
+                   const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
+                   int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,
+                   uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* stream);
+
+/*
+ * Fused LM head + top-16: logits = hidden W^T are produced tile by tile on the
+ * tensor cores and reduced to each row's top-16 on chip, so no logit reaches
+ * global memory (the head produces U_t, "DFlash's own logit").
+ *   hidden  device bf16 [M, d];  W device bf16 [V, d]
+ *   vals    device fp32 [M, 16];  idx device int32 [M, 16] (order as dflash2_topk)
+ *   workspace  device, >= dflash2_lmhead_topk_workspace(M, V, d) bytes, 256-byte
+ *              aligned; holds per-tile partial lists, fully rewritten per call.
+ * d % 64 == 0, M >= 1, V >= 16.
+ */
+size_t dflash2_lmhead_topk_workspace(int64_t M, int64_t V, int64_t d);
+int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
+                        int64_t V, int64_t d, float* vals, int32_t* idx, void* workspace,
+                        size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

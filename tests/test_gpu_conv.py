@@ -1,0 +1,54 @@
+"""Two-tap dynamic conv kernel vs the oracle: fp32 output within 1e-3 rel /
+1e-4 abs; bf16 output within one bf16 ulp of the oracle's value."""
+import numpy as np
+import pytest
+
+import oracle
+from draft_selection_dflash2_gb300 import api, synth
+from gpu_common import assert_close, bf, f32, handle, host  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def run(h, c, hs=None, y_fp32=True):
+    y = api.conv2tap(h, bf(c.x), bf(c.x_prev), bf(c.k0), bf(c.k1), bf(c.W_c),
+                     b_c=None if c.b_c is None else f32(c.b_c), hs=None if hs is None else bf(hs),
+                     y_fp32=y_fp32)
+    return host(y)
+
+
+@pytest.mark.parametrize("B,L,d,bias", [(1, 16, 2560, False), (2, 5, 192, True), (8, 16, 5120, False),
+                                        (3, 64, 512, True), (1, 1, 64, False)])
+def test_conv_fp32_matches_oracle(handle, B, L, d, bias):
+    c = synth.conv_inputs(B * 13 + L, B, L, d, with_bias=bias)
+    y = run(handle, c)
+    oy = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c, b_c=c.b_c)
+    assert_close(y, oy, what="y")
+
+
+def test_conv_bf16_within_one_ulp(handle):
+    c = synth.conv_inputs(5, 4, 16, 2560)
+    y = run(handle, c, y_fp32=False)
+    oy = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c)
+    ref = synth.bf16_to_f32(synth.bf16_bits(oy.astype(np.float32))).astype(np.float64)
+    got = synth.bf16_to_f32(y).astype(np.float64)
+    ulp = np.abs(ref) * 2.0**-7 + 1e-30
+    assert np.all(np.abs(got - ref) <= ulp)
+
+
+def test_conv_separate_hidden_state(handle):
+    c = synth.conv_inputs(6, 2, 16, 512, with_bias=True)
+    hs = synth.normal_bits(77, (2, 16, 512))
+    y = run(handle, c, hs=hs)
+    oy = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c, b_c=c.b_c, h_bits=hs)
+    assert_close(y, oy, what="y")
+
+
+def test_conv_identity_on_gpu(handle):
+    c = synth.conv_inputs(7, 2, 16, 256)
+    d = 256
+    c.k0[:] = synth.bf16_bits(np.ones(d, np.float32))
+    c.k1[:] = 0
+    c.W_c[:] = 0
+    y = run(handle, c, y_fp32=False)
+    assert np.array_equal(y, c.x)

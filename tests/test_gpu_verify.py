@@ -1,0 +1,86 @@
+"""Verification kernels vs the oracle.
+
+T = 0: acceptance lengths and emitted tokens bit-exact.
+T > 0: exact except sequences whose oracle decision margin is below 1e-4
+(relative), where fp32 exponentials may legitimately flip a draw; those are
+counted and must be rare.  Losslessness is checked statistically on V = 64."""
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+from draft_selection_dflash2_gb300 import api, synth
+from gpu_common import bf, f32, handle, host, i32  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+K = 16
+
+
+def draft(seed, B, L, V, T):
+    rng = np.random.default_rng(seed)
+    ci = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(L)]) for _ in range(B)])
+    ci = ci.astype(np.int32)
+    S = (rng.standard_normal((B, L, K, K)) * 2).astype(np.float32)
+    tok, slot, q, _ = oracle.walk(S, ci, temperature=float(np.float32(T)), seed=seed)
+    return tok, slot, q, ci
+
+
+@pytest.mark.parametrize("B,L,V", [(1, 8, 4096), (16, 16, 151936), (128, 16, 8200), (5, 1, 4099),
+                                   (9, 64, 1000)])
+def test_greedy_verify_exact(handle, B, L, V):
+    tok, slot, q, ci = draft(B + L, B, L, V, 0.0)
+    target = synth.target_planted(B * 3 + L, tok, V, agree=0.85)
+    acc, out = api.verify(handle, bf(target), i32(tok))
+    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci)
+    assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+@pytest.mark.parametrize("B,L,V,plant", [(64, 16, 8200, 12.0), (16, 16, 151936, 16.0), (40, 4, 4099, 6.0)])
+def test_sampled_verify_matches_oracle(handle, B, L, V, plant, T):
+    tok, slot, q, ci = draft(B * 7 + L, B, L, V, T)
+    target = synth.target_planted(B + 1, tok, V, agree=0.85, plant=plant)
+    Tf = float(np.float32(T))
+    acc, out = api.verify(handle, bf(target), i32(tok), i32(slot), f32(q), i32(ci), temperature=T,
+                          seed=11, offset=2)
+    oacc, oout, margin = oracle.verify(target, tok, slot, q, ci, temperature=Tf, seed=11, offset=2)
+    gacc, gout = host(acc), host(out)
+    near = margin < 1e-4
+    assert near.sum() <= max(1, B // 50)
+    ok = ~near
+    assert np.array_equal(gacc[ok], oacc[ok]) and np.array_equal(gout[ok], oout[ok])
+    assert handle.device_error() == 0
+
+
+def test_sampled_verify_is_lossless_on_gpu(handle):
+    V, L, n, T = 64, 2, 20000, 1.0
+    rng = np.random.default_rng(31)
+    t0 = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    rows = np.stack([t0, rng.standard_normal(V), rng.standard_normal(V)]).astype(np.float32)
+    target = np.broadcast_to(synth.bf16_bits(rows), (n, L + 1, V)).copy()
+    cand = rng.choice(V, K, replace=False).astype(np.int32)
+    ci = np.broadcast_to(cand, (n, L, K)).copy()
+    S = np.zeros((n, L, K, K), np.float32)
+    S[:] = (rng.standard_normal(K) * 2).astype(np.float32)
+    tok, slot, q = api.walk(handle, f32(S), i32(ci), temperature=T, seed=5)
+    acc, out = api.verify(handle, bf(target), tok, slot, q, i32(ci), temperature=T, seed=6)
+    first = host(out)[:, 0]
+    p = np.exp(synth.bf16_to_f32(target[0, 0]).astype(np.float64) / T)
+    p /= p.sum()
+    counts = np.bincount(first, minlength=V)
+    keep = p * n >= 5
+    obs, exp = counts[keep], p[keep] * n
+    if (~keep).any():
+        obs, exp = np.append(obs, counts[~keep].sum()), np.append(exp, p[~keep].sum() * n)
+    assert stats.chisquare(obs, exp).pvalue > 1e-4
+
+
+def test_greedy_mean_acceptance_closed_form_on_gpu(handle):
+    B, L, V, r = 4096, 16, 512, 0.85
+    rng = np.random.default_rng(8)
+    tok = rng.integers(0, V, (B, L)).astype(np.int32)
+    target = synth.target_planted(9, tok, V, agree=r, plant=12.0)
+    acc, _ = api.verify(handle, bf(target), i32(tok))
+    a = host(acc)
+    expect = 1.0 + sum(r**k for k in range(1, L + 1))
+    assert abs(a.mean() - expect) < 4 * a.std() / np.sqrt(B)

@@ -1,0 +1,55 @@
+"""Walk kernel vs the oracle on identical scores (conditional parity).
+
+Greedy choices are compared exactly.  Sampled choices are compared exactly
+except draws whose u*Z lies within 1e-12*Z of a CDF boundary (the two sides'
+fp64 exp may differ in the last bit); those are counted and must be absent."""
+import numpy as np
+import pytest
+
+import oracle
+from draft_selection_dflash2_gb300 import api
+from gpu_common import f32, handle, host, i32  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+K = 16
+
+
+def scores(seed, B, L, scale=1.0, ties=False):
+    rng = np.random.default_rng(seed)
+    S = (rng.standard_normal((B, L, K, K)) * scale).astype(np.float32)
+    if ties:
+        S[..., 5] = S[..., 2]
+        S[..., 11] = S[..., 2]
+    ci = rng.integers(0, 151936, (B, L, K)).astype(np.int32)
+    return S, ci
+
+
+@pytest.mark.parametrize("B,L", [(1, 8), (1, 16), (5, 3), (128, 16), (256, 16), (7, 64)])
+def test_greedy_walk_exact(handle, B, L):
+    S, ci = scores(B * 31 + L, B, L, ties=True)
+    tok, slot, q = api.walk(handle, f32(S), i32(ci))
+    otok, oslot, oq, _ = oracle.walk(S, ci)
+    assert np.array_equal(host(slot), oslot) and np.array_equal(host(tok), otok)
+    assert np.array_equal(host(q), oq)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 2.0])
+@pytest.mark.parametrize("B,L", [(1, 16), (128, 16), (33, 7)])
+def test_sampled_walk_exact(handle, B, L, T):
+    S, ci = scores(B + L + int(T * 10), B, L, scale=2.0)
+    Tf = float(np.float32(T))
+    for seed, offset in ((1, 0), (1, 7), (99, (5 << 32) + 3)):
+        tok, slot, q = api.walk(handle, f32(S), i32(ci), temperature=T, seed=seed, offset=offset)
+        otok, oslot, oq, margin = oracle.walk(S, ci, temperature=Tf, seed=seed, offset=offset)
+        close = margin < 1e-12
+        assert close.sum() == 0, "draws within 1e-12 of a CDF boundary"
+        assert np.array_equal(host(slot), oslot) and np.array_equal(host(tok), otok)
+        np.testing.assert_allclose(host(q), oq, rtol=2e-7, atol=1e-30)
+
+
+def test_walk_without_q(handle):
+    S, ci = scores(3, 4, 8)
+    tok, slot, q = api.walk(handle, f32(S), i32(ci), temperature=1.0, seed=3, want_q=False)
+    assert q is None
+    otok, oslot, _, _ = oracle.walk(S, ci, temperature=1.0, seed=3)
+    assert np.array_equal(host(slot), oslot)
