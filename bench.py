@@ -323,7 +323,7 @@ def run_gpu(args):
     if rank == 0 and args.e2e:
         line["e2e"] = run_e2e(torch, api, h, w, cyc, dev, args)
     if rank == 0 and args.cpu_baseline and world == 1:
-        line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=8)
+        line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=64)
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()

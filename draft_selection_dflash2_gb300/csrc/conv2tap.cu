@@ -7,110 +7,130 @@
 //   [c0; c1][m, :] = W_c h[m, :] (+ b_c)            W_c: [2G, d], G = d / 16
 //   y[m, ch] = (k0[ch] + c0[m, ch/16]) x[m, ch] + (k1[ch] + c1[m, ch/16]) xp[ch]
 //
-// One CTA owns one sequence b and a band of kGroups groups: it computes the
-// 2 * kGroups correction columns it needs for all L positions (the correction
-// never leaves shared memory), then applies the two-tap epilogue to the
-// band's 16 * kGroups channels.
+// One fused kernel: the correction is a [M, d] x [d, 2G] contraction on the
+// tensor cores (tcgen05 GEMM, fp32 accumulator in TMEM).  A CTA owns 128
+// positions x 32 groups: its B tile is W_c rows [g0, g0+32) (-> c0) stacked on
+// rows [G+g0, G+g0+32) (-> c1), so both coefficients of its 512 channels meet in
+// one accumulator.  The epilogue parks the 64 correction columns in shared
+// memory and then sweeps the 128 x 512 channel tile with coalesced 16-byte
+// loads of x_t / x_{t-1} and 16-byte stores of y; the correction never leaves
+// the SM.
 #include "common.cuh"
+#include "gemm_tc.cuh"
 #include "launch.h"
 
 namespace dflash2 {
 namespace {
 
-constexpr int kGroups = 16;            // groups per CTA band -> 256 channels
-constexpr int kCols = 2 * kGroups;     // correction columns per CTA
-constexpr int kKTile = 64;
-constexpr int kMaxConvL = 64;
+struct ConvEpi {
+  struct Params {
+    const uint16_t* x;        // [M, d]
+    const uint16_t* x_prev;   // [B, d]
+    const uint16_t* k0;       // [d]
+    const uint16_t* k1;       // [d]
+    const float* b_c;         // [2G] or null
+    void* y;                  // [M, d] bf16 or fp32
+    int y_is_fp32;
+    int M, L, d, G;
+  };
+  static constexpr int kGroups = 32;            // groups per CTA (512 channels)
+  static constexpr int kBN = 2 * kGroups;       // c0 | c1 columns
+  static constexpr int kPitch = kBN + 1;        // fp32 words per row in shared memory
+  static constexpr int kSmemBytes = 128 * kPitch * 4;
 
-__global__ void __launch_bounds__(256)
-    conv2tap_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ x_prev,
-                    const uint16_t* __restrict__ hs, const uint16_t* __restrict__ k0,
-                    const uint16_t* __restrict__ k1, const uint16_t* __restrict__ W_c,
-                    const float* __restrict__ b_c, int64_t L, int64_t d, void* __restrict__ y,
-                    int y_is_fp32) {
-  __shared__ float hsm[kMaxConvL][kKTile + 1];
-  __shared__ float wsm[kCols][kKTile + 1];
-  __shared__ float csm[kMaxConvL][kCols];
-  const int tid = threadIdx.x;
-  const int64_t b = blockIdx.y;
-  const int64_t G = d / 16;
-  const int64_t g0 = static_cast<int64_t>(blockIdx.x) * kGroups;
-  const int ng = static_cast<int>(G - g0 < kGroups ? G - g0 : kGroups);
-  const uint16_t* h = (hs ? hs : x) + b * L * d;
+  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, const Params& p, uint64_t* bar,
+                                uint64_t pol) {
+    const int g0 = blockIdx.y * kGroups;
+    tma_load_2d(dst, tm, k, g0, bar, pol);                                             // c0 rows
+    tma_load_2d(static_cast<uint8_t*>(dst) + kGroups * kTileRowBytes, tm, k, p.G + g0, bar, pol);  // c1 rows
+  }
 
-  // outputs (row, col) handled by this thread: col = tid % 32, rows tid/32 + 8 i
-  const int col = tid & (kCols - 1);
-  const int r0 = tid >> 5;
-  float acc[kMaxConvL / 8];
+  __device__ static void consume(const Params& p, uint8_t* smem, int, int row_local, int c, const float (&v)[32]) {
+    float* csm = reinterpret_cast<float*>(smem) + row_local * kPitch + c * kGroups;
+    const int g0 = blockIdx.y * kGroups;
 #pragma unroll
-  for (int i = 0; i < kMaxConvL / 8; ++i) acc[i] = 0.0f;
-  // correction column -> W_c row: col < kGroups -> c0 group g0+col, else c1 group g0+col-kGroups
-  const int cg = col < kGroups ? col : col - kGroups;
-  const bool col_ok = cg < ng;
-  const int64_t wrow = (col < kGroups ? 0 : G) + g0 + (col_ok ? cg : 0);
+    for (int i = 0; i < 32; ++i) {
+      const int g = g0 + i;
+      float bias = 0.0f;
+      if (p.b_c && g < p.G) bias = p.b_c[c * p.G + g];
+      csm[i] = v[i] + bias;
+    }
+  }
 
-  for (int64_t kt = 0; kt < d; kt += kKTile) {
-    for (int e = tid; e < L * kKTile; e += 256) {
-      const int r = e / kKTile, k = e % kKTile;
-      hsm[r][k] = bf16_bits_to_float(h[r * d + kt + k]);
-    }
-    for (int e = tid; e < kCols * kKTile; e += 256) {
-      const int cc = e / kKTile, k = e % kKTile;
-      const int cgg = cc < kGroups ? cc : cc - kGroups;
-      const int64_t wr = (cc < kGroups ? 0 : G) + g0 + (cgg < ng ? cgg : 0);
-      wsm[cc][k] = bf16_bits_to_float(W_c[wr * d + kt + k]);
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int k = 0; k < kKTile; ++k) {
-      const float w = wsm[col][k];
+  // 128 epilogue threads sweep the 128 x (16 * ng) channel tile, 8 channels each step.
+  __device__ static void finish(const Params& p, uint8_t* smem, int m0, int tid) {
+    const float* csm = reinterpret_cast<const float*>(smem);
+    const int g0 = blockIdx.y * kGroups;
+    const int ng = (p.G - g0 < kGroups) ? p.G - g0 : kGroups;
+    const int vec_per_row = 2 * ng;                 // 8-channel vectors per row
+    const int total = 128 * vec_per_row;
+    for (int e = tid; e < total; e += kEpiThreads) {
+      const int r = e / vec_per_row, cv = e % vec_per_row;
+      const int m = m0 + r;
+      if (m >= p.M) break;                          // rows are visited in order
+      const int gl = cv >> 1;
+      const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
+      const int t = m % p.L;
+      const int64_t b = m / p.L;
+      const uint4 xv = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.d + ch);
+      const uint16_t* prow = t > 0 ? p.x + static_cast<int64_t>(m - 1) * p.d : p.x_prev + b * p.d;
+      const uint4 pv = *reinterpret_cast<const uint4*>(prow + ch);
+      const uint4 a0v = *reinterpret_cast<const uint4*>(p.k0 + ch);
+      const uint4 a1v = *reinterpret_cast<const uint4*>(p.k1 + ch);
+      const float c0 = csm[r * kPitch + gl];
+      const float c1 = csm[r * kPitch + kGroups + gl];
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, pw[4] = {pv.x, pv.y, pv.z, pv.w};
+      const uint32_t k0w[4] = {a0v.x, a0v.y, a0v.z, a0v.w}, k1w[4] = {a1v.x, a1v.y, a1v.z, a1v.w};
+      float out[8];
 #pragma unroll
-      for (int i = 0; i < kMaxConvL / 8; ++i) {
-        const int r = r0 + 8 * i;
-        if (r < L) acc[i] = fmaf(hsm[r][k], w, acc[i]);
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int sh = h * 16;
+          const float xt = bf16_bits_to_float((xw[q] >> sh) & 0xFFFFu);
+          const float xp = bf16_bits_to_float((pw[q] >> sh) & 0xFFFFu);
+          const float a0 = bf16_bits_to_float((k0w[q] >> sh) & 0xFFFFu) + c0;
+          const float a1 = bf16_bits_to_float((k1w[q] >> sh) & 0xFFFFu) + c1;
+          out[2 * q + h] = fmaf(a0, xt, a1 * xp);
+        }
+      }
+      const int64_t o = static_cast<int64_t>(m) * p.d + ch;
+      if (p.y_is_fp32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+        dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+      } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q]));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q + 1]));
+          w[q] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    __syncthreads();
   }
-#pragma unroll
-  for (int i = 0; i < kMaxConvL / 8; ++i) {
-    const int r = r0 + 8 * i;
-    if (r < L) csm[r][col] = acc[i] + ((b_c && col_ok) ? b_c[wrow] : 0.0f);
-  }
-  __syncthreads();
-
-  // epilogue: 16 * ng channels x L positions
-  const int nch = 16 * ng;
-  const int64_t ch0 = 16 * g0;
-  for (int e = tid; e < L * nch; e += 256) {
-    const int r = e / nch, cl = e % nch;
-    const int64_t ch = ch0 + cl;
-    const int g = cl >> 4;
-    const int64_t m = b * L + r;
-    const float xt = bf16_bits_to_float(x[m * d + ch]);
-    const float xp = bf16_bits_to_float(r > 0 ? x[(m - 1) * d + ch] : x_prev[b * d + ch]);
-    const float a0 = bf16_bits_to_float(k0[ch]) + csm[r][g];
-    const float a1 = bf16_bits_to_float(k1[ch]) + csm[r][kGroups + g];
-    const float v = fmaf(a0, xt, a1 * xp);
-    if (y_is_fp32)
-      static_cast<float*>(y)[m * d + ch] = v;
-    else
-      static_cast<__nv_bfloat16*>(y)[m * d + ch] = __float2bfloat16_rn(v);
-  }
-}
+};
 
 }  // namespace
 
 cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* hs,
                             const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
-                            int y_is_fp32, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
-  if (L > kMaxConvL || d % kKTile != 0 || B > 65535) return cudaErrorInvalidValue;
+                            int y_is_fp32, uint32_t* err, cudaStream_t stream) {
+  const int64_t M = B * L;
+  if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const int64_t G = d / 16;
-  dim3 grid(static_cast<unsigned>((G + kGroups - 1) / kGroups), static_cast<unsigned>(B));
-  conv2tap_kernel<<<grid, 256, 0, stream>>>(x, x_prev, hs, k0, k1, W_c, b_c, L, d, y, y_is_fp32);
-  return cudaGetLastError();
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, hs ? hs : x, M, d, d, 128) ||
+      !make_tmap_bf16_2d(&tb, W_c, 2 * G, d, d, ConvEpi::kGroups))
+    return cudaErrorInvalidValue;
+  ConvEpi::Params p{x, x_prev, k0, k1, b_c, y, y_is_fp32, static_cast<int>(M), static_cast<int>(L),
+                    static_cast<int>(d), static_cast<int>(G)};
+  const int grid_n = static_cast<int>((G + ConvEpi::kGroups - 1) / ConvEpi::kGroups);
+  return launch_tc_gemm<ConvEpi::kBN, 4, ConvEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d), grid_n, p,
+                                                  err, stream);
 }
 
 }  // namespace dflash2

@@ -2,8 +2,9 @@
 // Drafting Parallel", "A Lightweight Path Selector", score equation
 // S_t(a,b) = U_t(b) + <A(a) (.) H(h_t), B(b)>).
 //
-// gate_kernel      H = sigmoid(W_H h + b_H): one [B*L, d] x [d, 256] contraction,
-//                  fp32 accumulate, sigmoid fused in the epilogue.
+// gate             H = sigmoid(W_H h + b_H): one [B*L, d] x [d, 256] contraction on
+//                  the tensor cores (tcgen05 + TMA, fp32 in TMEM), sigmoid fused
+//                  in the epilogue.
 // pair_kernel      one CTA per block position (b, t): gathers the 16 predecessor
 //                  rows of A and the 16 candidate rows of B (512 B each) with
 //                  16-byte loads, forms G = A_pred (.) H_t in fp32 shared memory,
@@ -11,71 +12,47 @@
 //                  tile per thread over 16 interleaved slices of r, reduced by a
 //                  15-shuffle reduce-scatter.
 #include "common.cuh"
+#include "gemm_tc.cuh"
 #include "launch.h"
 
 namespace dflash2 {
 namespace {
 
 // ---------------------------------------------------------------------------
-// gate: C[m, n] = sum_k h[m, k] W[n, k]; H = sigmoid(C + b)
+// gate: H = sigmoid(h W_H^T + b) on the tensor cores (tcgen05, fp32 in TMEM),
+// 128 positions x 64 gate channels per CTA, sigmoid fused in the epilogue.
 // ---------------------------------------------------------------------------
-constexpr int kGTileM = 64, kGTileN = 64, kGTileK = 32;
+struct GateEpi {
+  struct Params {
+    float* gate;          // [M, 256]
+    const float* bias;    // [256] or null
+    int M;
+  };
+  static constexpr int kBN = 64;
+  static constexpr int kSmemBytes = 0;
 
-__global__ void __launch_bounds__(256) gate_kernel(const uint16_t* __restrict__ hs,
-                                                   const uint16_t* __restrict__ W,
-                                                   const float* __restrict__ bias, int64_t M,
-                                                   int64_t d, float* __restrict__ gate) {
-  __shared__ float As[kGTileK][kGTileM + 4];
-  __shared__ float Ws[kGTileK][kGTileN + 4];
-  const int tid = threadIdx.x;
-  const int tm = tid >> 4, tn = tid & 15;          // 16 x 16 threads, 4 x 4 outputs each
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kGTileM;
-  const int n0 = blockIdx.y * kGTileN;
-  float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < d; k0 += kGTileK) {
-    // 64 rows x 32 k of each operand: 256 threads x 8 elements (one 16-byte load)
-    {
-      const int r = tid >> 2, kc = (tid & 3) * 8;
-      const int64_t gm = m0 + r;
-      uint4 va = make_uint4(0, 0, 0, 0);
-      if (gm < M) va = *reinterpret_cast<const uint4*>(hs + gm * d + k0 + kc);
-      const uint4 vw = *reinterpret_cast<const uint4*>(W + static_cast<int64_t>(n0 + r) * d + k0 + kc);
-      const uint32_t a[4] = {va.x, va.y, va.z, va.w}, w[4] = {vw.x, vw.y, vw.z, vw.w};
+  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, const Params&, uint64_t* bar,
+                                uint64_t pol) {
+    tma_load_2d(dst, tm, k, blockIdx.y * kBN, bar, pol);
+  }
+  __device__ static void consume(const Params& p, uint8_t*, int m0, int row_local, int c, const float (&v)[32]) {
+    const int row = m0 + row_local;
+    if (row >= p.M) return;
+    const int n0 = blockIdx.y * kBN + c * 32;
+    float4* dst = reinterpret_cast<float4*>(p.gate + static_cast<int64_t>(row) * kEmbed + n0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        As[kc + 2 * q][r] = bf16_bits_to_float(a[q] & 0xFFFFu);
-        As[kc + 2 * q + 1][r] = bf16_bits_to_float(a[q] >> 16);
-        Ws[kc + 2 * q][r] = bf16_bits_to_float(w[q] & 0xFFFFu);
-        Ws[kc + 2 * q + 1][r] = bf16_bits_to_float(w[q] >> 16);
+    for (int i = 0; i < 32; i += 4) {
+      float o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float z = v[i + j] + (p.bias ? p.bias[n0 + i + j] : 0.0f);
+        o[j] = 1.0f / (1.0f + expf(-z));
       }
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kGTileK; ++kk) {
-      float a[4], w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][tm * 4 + i];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = Ws[kk][tn * 4 + i];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jx = 0; jx < 4; ++jx) acc[i][jx] = fmaf(a[i], w[jx], acc[i][jx]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t gm = m0 + tm * 4 + i;
-    if (gm >= M) continue;
-#pragma unroll
-    for (int jx = 0; jx < 4; ++jx) {
-      const int n = n0 + tn * 4 + jx;
-      const float z = acc[i][jx] + (bias ? bias[n] : 0.0f);
-      gate[gm * kEmbed + n] = 1.0f / (1.0f + expf(-z));
+      dst[i / 4] = make_float4(o[0], o[1], o[2], o[3]);
     }
   }
-}
+  __device__ static void finish(const Params&, uint8_t*, int, int) {}
+};
 
 // ---------------------------------------------------------------------------
 // pair scores
@@ -176,12 +153,14 @@ __global__ void __launch_bounds__(256) pair_kernel(const int32_t* __restrict__ c
 }  // namespace
 
 cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_H, int64_t M,
-                        int64_t d, float* gate, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
-  if (d % kGTileK != 0) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>((M + kGTileM - 1) / kGTileM), kEmbed / kGTileN);
-  gate_kernel<<<grid, 256, 0, stream>>>(hs, W_H, b_H, M, d, gate);
-  return cudaGetLastError();
+                        int64_t d, float* gate, uint32_t* err, cudaStream_t stream) {
+  if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_H, kEmbed, d, d, GateEpi::kBN))
+    return cudaErrorInvalidValue;
+  GateEpi::Params p{gate, b_H, static_cast<int>(M)};
+  return launch_tc_gemm<GateEpi::kBN, 6, GateEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d),
+                                                  kEmbed / GateEpi::kBN, p, err, stream);
 }
 
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,

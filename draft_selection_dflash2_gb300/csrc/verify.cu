@@ -141,16 +141,22 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nvec = V >> 3;
   const uint4* rv = reinterpret_cast<const uint4*>(row);
-  float m = -INFINITY, acc = 0.0f;
+  // Per thread: running max m and sum acc of 2^((l - m) c); each 8-element
+  // vector is summed in fp32 and added in fp64, so the row sum keeps ~1e-7
+  // relative accuracy.
+  float m = -INFINITY;
+  double acc = 0.0;
   auto absorb = [&](const uint4& v) {
     const float vm = bf16_bits_to_float(vec_max_bits(v));
     if (vm > m) {
-      acc *= fast_exp2((m - vm) * c);
+      acc *= static_cast<double>(fast_exp2((m - vm) * c));
       m = vm;
     }
     const float mc = m * c;
+    float vs = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc += fast_exp2(fmaf(bf16_bits_to_float(lane_bits(v, k)), c, -mc));
+    for (int k = 0; k < 8; ++k) vs += fast_exp2(fmaf(bf16_bits_to_float(lane_bits(v, k)), c, -mc));
+    acc += static_cast<double>(vs);
   };
   int64_t i = threadIdx.x;
   for (; i + 3 * kVThreads < nvec; i += 4 * kVThreads) {
@@ -164,10 +170,10 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   for (int64_t e = nvec * 8 + threadIdx.x; e < V; e += kVThreads) {
     const float x = bf16_bits_to_float(row[e]);
     if (x > m) {
-      acc *= fast_exp2((m - x) * c);
+      acc *= static_cast<double>(fast_exp2((m - x) * c));
       m = x;
     }
-    acc += fast_exp2((x - m) * c);
+    acc += static_cast<double>(fast_exp2((x - m) * c));
   }
   // combine (m, acc) over the block; the sum is carried in fp64
   float wm = m;
@@ -178,7 +184,7 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   float M = s.m[0];
 #pragma unroll
   for (int w = 1; w < kVWarps; ++w) M = fmaxf(M, s.m[w]);
-  double z = (m == -INFINITY) ? 0.0 : static_cast<double>(acc) * static_cast<double>(fast_exp2((m - M) * c));
+  double z = (m == -INFINITY) ? 0.0 : acc * static_cast<double>(fast_exp2((m - M) * c));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
   if (lane == 0) s.z[warp] = z;

@@ -125,14 +125,14 @@ def pair_scores(cand_idx, cand_val, last_verified, H, A_bits, B_bits, nthreads=N
 
 
 def walk(S, cand_idx, temperature=0.0, seed=0, offset=0, nthreads=None):
-    """S: f32 [B, L, K, K] -> (draft_tok, draft_slot, draft_q, margin)."""
+    """S: f32 [B, L, K, K] -> (draft_tok, draft_slot, draft_q, margin [B, L] per step)."""
     Sf = _c(S, np.float32)
     ci = _c(cand_idx, np.int32)
     B, L, K, _ = Sf.shape
     tok = np.zeros((B, L), np.int32)
     slot = np.zeros((B, L), np.int32)
     q = np.zeros((B, L, K), np.float32)
-    margin = np.zeros(B, np.float64)
+    margin = np.zeros((B, L), np.float64)
     _load().oracle_walk(_p(Sf), _p(ci), B, L, K, float(temperature), seed, offset, _p(tok), _p(slot),
                         _p(q), _p(margin), nthreads or default_threads())
     return tok, slot, q, margin
@@ -156,7 +156,10 @@ def conv2tap(x_bits, x_prev_bits, k0_bits, k1_bits, W_c_bits, b_c=None, h_bits=N
 
 def verify(target_bits, draft_tok, draft_slot, draft_q, cand_idx, temperature=0.0, seed=0, offset=0,
            V=None, nthreads=None):
-    """target: uint16 [B, L+1, ld] -> (accept_len [B], out_tok [B, L+1], margin [B])."""
+    """target: uint16 [B, L+1, ld] -> (accept_len [B], out_tok [B, L+1], margin [B, 2]).
+
+    margin[:, 0]: smallest relative accept-test margin; margin[:, 1]: smallest
+    draw margin relative to the total mass (both +inf at temperature 0)."""
     tg = _c(target_bits, np.uint16)
     dt = _c(draft_tok, np.int32)
     ds = _c(draft_slot, np.int32)
@@ -168,7 +171,7 @@ def verify(target_bits, draft_tok, draft_slot, draft_q, cand_idx, temperature=0.
     V = ld if V is None else V
     acc = np.zeros(B, np.int32)
     out = np.zeros((B, L + 1), np.int32)
-    margin = np.zeros(B, np.float64)
+    margin = np.zeros((B, 2), np.float64)
     _load().oracle_verify(_p(tg), ld, _p(dt), _p(ds), _p(dq), _p(ci), B, L, K, V, float(temperature),
                           seed, offset, _p(acc), _p(out), _p(margin), nthreads or default_threads())
     return acc, out, margin

@@ -231,9 +231,9 @@ int oracle_pair_scores(const int32_t* cand_idx, const float* cand_val,
 //                     q[b, t, j] = w_j / Z.
 // S: [B, L, K, K] fp32 (the walk reads scores at the precision they are stored);
 // outputs draft_tok, draft_slot: [B, L]; q: [B, L, K] or null;
-// margin: [B] or null -- per sequence the smallest decision margin met on the
-// path (greedy: best - runner-up; sampled: distance of u*Z to the nearest CDF
-// boundary of the chosen slot, relative to Z).
+// margin: [B, L] or null -- the decision margin of every step (greedy: best -
+// runner-up; sampled: distance of u*Z to the nearest CDF boundary of the chosen
+// slot, relative to Z).
 // ---------------------------------------------------------------------------
 void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int64_t K,
                  double temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
@@ -241,8 +241,8 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
 #pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
   for (int64_t b = 0; b < B; ++b) {
     int64_t prev = 0;
-    double min_margin = std::numeric_limits<double>::infinity();
     for (int64_t t = 0; t < L; ++t) {
+      double step_margin = 0.0;
       const int64_t row = (t == 0) ? 0 : prev;
       const float* s = S + ((b * L + t) * K + row) * K;
       int64_t best = 0;
@@ -254,7 +254,7 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
         double runner = -std::numeric_limits<double>::infinity();
         for (int64_t j = 0; j < K; ++j)
           if (j != best) runner = std::max(runner, static_cast<double>(s[j]));
-        min_margin = std::min(min_margin, static_cast<double>(s[best]) - runner);
+        step_margin = static_cast<double>(s[best]) - runner;
         if (q)
           for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = (j == chosen) ? 1.0f : 0.0f;
       } else {
@@ -282,15 +282,15 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
             }
         double gap = cdf[chosen] - target;
         if (chosen > 0) gap = std::min(gap, target - cdf[chosen - 1]);
-        min_margin = std::min(min_margin, gap / Z);
+        step_margin = gap / Z;
         if (q)
           for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = static_cast<float>(w[j] / Z);
       }
       draft_slot[b * L + t] = static_cast<int32_t>(chosen);
       draft_tok[b * L + t] = cand_idx[(b * L + t) * K + chosen];
+      if (margin) margin[b * L + t] = step_margin;
       prev = chosen;
     }
-    if (margin) margin[b] = min_margin;
   }
 }
 
@@ -349,8 +349,10 @@ void oracle_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* 
 //   uniform24(seed, b, L, 2, offset); accept_len = L + 1.
 // target: [B, L + 1, ld] bf16 (row (b, t) starts at (b * (L + 1) + t) * ld);
 // out_tok: [B, L + 1], -1 after the last emitted token.
-// margin: [B] or null -- the smallest relative decision margin met on the path
-// (T > 0 only; +inf at T = 0, whose decisions are exact).
+// margin: [B, 2] or null -- T > 0 only (+inf at T = 0, whose decisions are
+// exact): [0] the smallest |u q - p(x)| / p(x) over the accept tests on the
+// path, [1] the smallest distance of a draw's target mass to the CDF boundaries
+// of the drawn token, relative to the total mass.
 // ---------------------------------------------------------------------------
 void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                    const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
@@ -361,7 +363,8 @@ void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
   for (int64_t b = 0; b < B; ++b) {
     int32_t* out = out_tok + b * (L + 1);
     for (int64_t t = 0; t <= L; ++t) out[t] = -1;
-    double min_margin = std::numeric_limits<double>::infinity();
+    double accept_margin = std::numeric_limits<double>::infinity();
+    double draw_margin = std::numeric_limits<double>::infinity();
     int64_t n = L;
     int32_t last = -1;
     if (temperature <= 0.0) {
@@ -413,7 +416,7 @@ void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
           prev_run = run;
         }
         double gap = std::min(run - target_mass, target_mass - prev_run);
-        min_margin = std::min(min_margin, gap / total);
+        draw_margin = std::min(draw_margin, gap / total);
         return static_cast<int32_t>(chosen);
       };
       n = L;
@@ -424,7 +427,7 @@ void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
         const double px = (x >= 0 && x < V) ? p[x] : 0.0;
         const double u = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 1, offset);
         const double lhs = u * qx;
-        min_margin = std::min(min_margin, std::fabs(lhs - px) / std::max(px, 1e-300));
+        accept_margin = std::min(accept_margin, std::fabs(lhs - px) / std::max(px, 1e-300));
         if (lhs < px) continue;
         std::vector<double> resid(p);
         for (int64_t j = 0; j < K; ++j) {
@@ -444,7 +447,10 @@ void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
     for (int64_t t = 0; t < n; ++t) out[t] = draft_tok[b * L + t];
     out[n] = last;
     accept_len[b] = static_cast<int32_t>(n + 1);
-    if (margin) margin[b] = min_margin;
+    if (margin) {
+      margin[2 * b] = accept_margin;
+      margin[2 * b + 1] = draw_margin;
+    }
   }
 }
 

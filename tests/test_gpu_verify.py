@@ -16,6 +16,17 @@ pytestmark = pytest.mark.gpu
 K = 16
 
 
+# The GPU forms p(x) and the residual CDF from fp32 exponentials summed in
+# fp64 (relative error ~1e-6); decisions closer than that to their boundary may
+# legitimately flip and are excused (counted).
+ACCEPT_MARGIN = 1e-5     # |u q - p(x)| / p(x)
+DRAW_MARGIN = 2e-6       # distance to the drawn token's CDF interval / total mass
+
+
+def excused(margin):
+    return (margin[:, 0] < ACCEPT_MARGIN) | (margin[:, 1] < DRAW_MARGIN)
+
+
 def draft(seed, B, L, V, T):
     rng = np.random.default_rng(seed)
     ci = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(L)]) for _ in range(B)])
@@ -25,13 +36,24 @@ def draft(seed, B, L, V, T):
     return tok, slot, q, ci
 
 
+def padded(target, V):
+    """Target logits with the leading dimension rounded up to a multiple of 8;
+    the padding holds large values that must never be read."""
+    ld = (V + 7) // 8 * 8
+    if ld == V:
+        return target
+    out = np.full(target.shape[:2] + (ld,), synth.bf16_bits(np.float32(1e4)), np.uint16)
+    out[..., :V] = target
+    return out
+
+
 @pytest.mark.parametrize("B,L,V", [(1, 8, 4096), (16, 16, 151936), (128, 16, 8200), (5, 1, 4099),
                                    (9, 64, 1000)])
 def test_greedy_verify_exact(handle, B, L, V):
     tok, slot, q, ci = draft(B + L, B, L, V, 0.0)
-    target = synth.target_planted(B * 3 + L, tok, V, agree=0.85)
-    acc, out = api.verify(handle, bf(target), i32(tok))
-    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci)
+    target = padded(synth.target_planted(B * 3 + L, tok, V, agree=0.85), V)
+    acc, out = api.verify(handle, bf(target), i32(tok), V=V)
+    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci, V=V)
     assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
 
 
@@ -39,14 +61,14 @@ def test_greedy_verify_exact(handle, B, L, V):
 @pytest.mark.parametrize("B,L,V,plant", [(64, 16, 8200, 12.0), (16, 16, 151936, 16.0), (40, 4, 4099, 6.0)])
 def test_sampled_verify_matches_oracle(handle, B, L, V, plant, T):
     tok, slot, q, ci = draft(B * 7 + L, B, L, V, T)
-    target = synth.target_planted(B + 1, tok, V, agree=0.85, plant=plant)
+    target = padded(synth.target_planted(B + 1, tok, V, agree=0.85, plant=plant), V)
     Tf = float(np.float32(T))
     acc, out = api.verify(handle, bf(target), i32(tok), i32(slot), f32(q), i32(ci), temperature=T,
-                          seed=11, offset=2)
-    oacc, oout, margin = oracle.verify(target, tok, slot, q, ci, temperature=Tf, seed=11, offset=2)
+                          seed=11, offset=2, V=V)
+    oacc, oout, margin = oracle.verify(target, tok, slot, q, ci, temperature=Tf, seed=11, offset=2, V=V)
     gacc, gout = host(acc), host(out)
-    near = margin < 1e-4
-    assert near.sum() <= max(1, B // 50)
+    near = excused(margin)
+    assert near.sum() <= max(2, B // 10)
     ok = ~near
     assert np.array_equal(gacc[ok], oacc[ok]) and np.array_equal(gout[ok], oout[ok])
     assert handle.device_error() == 0

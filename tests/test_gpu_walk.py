@@ -41,7 +41,7 @@ def test_sampled_walk_exact(handle, B, L, T):
     for seed, offset in ((1, 0), (1, 7), (99, (5 << 32) + 3)):
         tok, slot, q = api.walk(handle, f32(S), i32(ci), temperature=T, seed=seed, offset=offset)
         otok, oslot, oq, margin = oracle.walk(S, ci, temperature=Tf, seed=seed, offset=offset)
-        close = margin < 1e-12
+        close = margin < 1e-12          # per step
         assert close.sum() == 0, "draws within 1e-12 of a CDF boundary"
         assert np.array_equal(host(slot), oslot) and np.array_equal(host(tok), otok)
         np.testing.assert_allclose(host(q), oq, rtol=2e-7, atol=1e-30)
