@@ -57,57 +57,75 @@ struct ConvEpi {
     }
   }
 
-  // 128 epilogue threads sweep the 128 x (16 * ng) channel tile, 8 channels each step.
+  // All 192 threads sweep the 128 x (16 * ng) channel tile in 8-channel vectors;
+  // each thread issues the loads of kUnroll vectors before using any of them.
+  static constexpr int kUnroll = 4;
+
   __device__ static void finish(const Params& p, uint8_t* smem, int m0, int tid) {
     const float* csm = reinterpret_cast<const float*>(smem);
     const int g0 = blockIdx.y * kGroups;
     const int ng = (p.G - g0 < kGroups) ? p.G - g0 : kGroups;
     const int vec_per_row = 2 * ng;                 // 8-channel vectors per row
-    const int total = 128 * vec_per_row;
-    for (int e = tid; e < total; e += kEpiThreads) {
-      const int r = e / vec_per_row, cv = e % vec_per_row;
-      const int m = m0 + r;
-      if (m >= p.M) break;                          // rows are visited in order
-      const int gl = cv >> 1;
-      const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
-      const int t = m % p.L;
-      const int64_t b = m / p.L;
-      const uint4 xv = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.d + ch);
-      const uint16_t* prow = t > 0 ? p.x + static_cast<int64_t>(m - 1) * p.d : p.x_prev + b * p.d;
-      const uint4 pv = *reinterpret_cast<const uint4*>(prow + ch);
-      const uint4 a0v = *reinterpret_cast<const uint4*>(p.k0 + ch);
-      const uint4 a1v = *reinterpret_cast<const uint4*>(p.k1 + ch);
-      const float c0 = csm[r * kPitch + gl];
-      const float c1 = csm[r * kPitch + kGroups + gl];
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, pw[4] = {pv.x, pv.y, pv.z, pv.w};
-      const uint32_t k0w[4] = {a0v.x, a0v.y, a0v.z, a0v.w}, k1w[4] = {a1v.x, a1v.y, a1v.z, a1v.w};
-      float out[8];
+    const int rows = (p.M - m0 < 128) ? p.M - m0 : 128;
+    const int total = rows * vec_per_row;
+    for (int e0 = tid; e0 < total; e0 += kUnroll * kGemmThreads) {
+      uint4 xv[kUnroll], pv[kUnroll], a0v[kUnroll], a1v[kUnroll];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int sh = h * 16;
-          const float xt = bf16_bits_to_float((xw[q] >> sh) & 0xFFFFu);
-          const float xp = bf16_bits_to_float((pw[q] >> sh) & 0xFFFFu);
-          const float a0 = bf16_bits_to_float((k0w[q] >> sh) & 0xFFFFu) + c0;
-          const float a1 = bf16_bits_to_float((k1w[q] >> sh) & 0xFFFFu) + c1;
-          out[2 * q + h] = fmaf(a0, xt, a1 * xp);
-        }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int e = e0 + u * kGemmThreads;
+        if (e >= total) continue;
+        const int r = e / vec_per_row, cv = e % vec_per_row;
+        const int m = m0 + r;
+        const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
+        const int t = m % p.L;
+        const uint16_t* prow = t > 0 ? p.x + static_cast<int64_t>(m - 1) * p.d : p.x_prev + (m / p.L) * static_cast<int64_t>(p.d);
+        xv[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.d + ch);
+        pv[u] = *reinterpret_cast<const uint4*>(prow + ch);
+        a0v[u] = __ldg(reinterpret_cast<const uint4*>(p.k0 + ch));
+        a1v[u] = __ldg(reinterpret_cast<const uint4*>(p.k1 + ch));
       }
-      const int64_t o = static_cast<int64_t>(m) * p.d + ch;
-      if (p.y_is_fp32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
-        dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-        dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-      } else {
-        uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int e = e0 + u * kGemmThreads;
+        if (e >= total) continue;
+        const int r = e / vec_per_row, cv = e % vec_per_row;
+        const int m = m0 + r;
+        const int gl = cv >> 1;
+        const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
+        const float c0 = csm[r * kPitch + gl];
+        const float c1 = csm[r * kPitch + kGroups + gl];
+        const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+        const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+        const uint32_t k0w[4] = {a0v[u].x, a0v[u].y, a0v[u].z, a0v[u].w};
+        const uint32_t k1w[4] = {a1v[u].x, a1v[u].y, a1v[u].z, a1v[u].w};
+        float out[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q]));
-          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q + 1]));
-          w[q] = lo | (hi << 16);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int sh = h * 16;
+            const float xt = bf16_bits_to_float((xw[q] >> sh) & 0xFFFFu);
+            const float xp = bf16_bits_to_float((pw[q] >> sh) & 0xFFFFu);
+            const float a0 = bf16_bits_to_float((k0w[q] >> sh) & 0xFFFFu) + c0;
+            const float a1 = bf16_bits_to_float((k1w[q] >> sh) & 0xFFFFu) + c1;
+            out[2 * q + h] = fmaf(a0, xt, a1 * xp);
+          }
         }
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+        const int64_t o = static_cast<int64_t>(m) * p.d + ch;
+        if (p.y_is_fp32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+          dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+          dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q]));
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q + 1]));
+            w[q] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
     }
   }
@@ -129,7 +147,7 @@ cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uin
   ConvEpi::Params p{x, x_prev, k0, k1, b_c, y, y_is_fp32, static_cast<int>(M), static_cast<int>(L),
                     static_cast<int>(d), static_cast<int>(G)};
   const int grid_n = static_cast<int>((G + ConvEpi::kGroups - 1) / ConvEpi::kGroups);
-  return launch_tc_gemm<ConvEpi::kBN, 4, ConvEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d), grid_n, p,
+  return launch_tc_gemm<ConvEpi::kBN, 3, ConvEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d), grid_n, p,
                                                   err, stream);
 }
 

@@ -10,7 +10,7 @@
 //                 producer, then commits the finished accumulator.
 //   warps 2..5    epilogue: tcgen05.ld of the accumulator, 32 columns at a time
 //                 (warp w reads TMEM lanes 32 (w % 4) .. +31 = its 32 rows), fed
-//                 to Epi::consume; Epi::finish runs after all four warps are done.
+//                 to Epi::consume.  Epi::finish then runs on all 192 threads.
 // Every mbarrier wait is bounded; a timeout raises DFLASH2_DEVERR_TIMEOUT and the
 // CTA drains its in-flight copies and MMAs before freeing TMEM and exiting.
 #pragma once
@@ -20,8 +20,6 @@
 namespace dflash2 {
 
 constexpr int kGemmThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr int kEpiBarrier = 1;        // named barrier id of the epilogue warps
 
 template <int BN, int STAGES>
 struct GemmLayout {
@@ -37,7 +35,7 @@ struct GemmLayout {
 };
 
 template <int BN, int STAGES, class Epi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 2)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int K,
                    const typename Epi::Params p, uint32_t* __restrict__ err) {
   using Lay = GemmLayout<BN, STAGES>;
@@ -136,10 +134,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     tc_fence_before();
-    named_bar_sync(kEpiBarrier, kEpiThreads);
-    if (ok) Epi::finish(p, epi_smem, m0, threadIdx.x - 64);
   }
-
+  // Epi::finish runs on all six warps (the producer and MMA warps are idle by now).
+  __syncthreads();
+  if (!*abort_flag) Epi::finish(p, epi_smem, m0, threadIdx.x);
   __syncthreads();
   if (warp == 1) {
     if (lane == 0) {

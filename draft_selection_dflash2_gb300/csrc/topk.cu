@@ -28,24 +28,29 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageBytes = 8192;                    // 4096 logits per stage
+constexpr int kStageBytes = 16384;                   // 8192 logits per stage
 constexpr int kStageElems = kStageBytes / 2;
+constexpr int kVecPerThread = kStageElems / 8 / kThreads;   // 4 x 16-byte vectors
 constexpr int kStages = 4;
 constexpr int kCompactAt = 64;                       // fold the buffer beyond this many
-constexpr int kCandCap = kStageElems + kCompactAt + 64;
+constexpr int kCandCap = 512 + kCompactAt;           // overflow -> the chunk is rescanned
+constexpr int kRescanVecs = 64;                      // vectors per rescan slice (512 logits)
 
 struct TopkSmem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];
+  alignas(128) uint8_t stage[kStages][kStageBytes];   // 1-D bulk copies need 16-byte alignment
   uint64_t cand[kCandCap];
   uint64_t top[kTopK];        // running top-16, descending
   uint64_t warp_top[kWarps][kTopK];
   uint64_t full_bar[kStages];
   uint64_t thr_key;           // top[15] (0 while fewer than 16 seen)
+  unsigned long long init_thr;  // lower bound used for a chunk that starts with no threshold
   int count;
+  int count0;                 // count at the start of the current chunk
+  int overflow;
 };
 
-// Folds cand[0..n) into s.top using every warp; leaves s.thr_key updated.
-// Must be called by all threads of the CTA (contains __syncthreads).
+// Folds cand[0..n) into s.top using every warp; leaves s.thr_key updated and
+// s.count = 0.  Must be called by all threads of the CTA (contains __syncthreads).
 __device__ void fold_candidates(TopkSmem& s, int n, int warp, int lane) {
   if (n <= 32) {
     if (warp == 0) {
@@ -54,6 +59,7 @@ __device__ void fold_candidates(TopkSmem& s, int n, int warp, int lane) {
       top = warp_merge_top16(top, x, lane);
       if (lane < kTopK) s.top[lane] = top;
       if (lane == kTopK - 1) s.thr_key = top;
+      if (lane == 0) s.count = 0;
     }
     __syncthreads();
     return;
@@ -74,13 +80,17 @@ __device__ void fold_candidates(TopkSmem& s, int n, int warp, int lane) {
     }
     if (lane < kTopK) s.top[lane] = acc;
     if (lane == kTopK - 1) s.thr_key = acc;
+    if (lane == 0) s.count = 0;
   }
   __syncthreads();
 }
 
 __device__ __forceinline__ void push_candidate(TopkSmem& s, uint64_t key) {
   const int slot = atomicAdd(&s.count, 1);
-  s.cand[slot] = key;   // slot < kCandCap by construction (see kCandCap)
+  if (slot < kCandCap)
+    s.cand[slot] = key;
+  else
+    s.overflow = 1;   // the chunk is rolled back and rescanned in slices
 }
 
 // Examines 8 logits (one 16-byte vector) whose first id is `id0`.
@@ -97,14 +107,15 @@ __device__ __forceinline__ void scan_vector(TopkSmem& s, uint4 v, uint32_t id0, 
   }
 }
 
-// Max of 8 bf16 values (bf16x2 max; a NaN never wins), as float.
-__device__ __forceinline__ float vec_max(uint4 v) {
+// Max of 8 bf16 values (bf16x2 max; a NaN never wins) as bf16 bits.
+__device__ __forceinline__ uint32_t vec_max_bits(uint4 v) {
   __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&v.x);
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v.y);
   __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&v.z);
   __nv_bfloat162 d = *reinterpret_cast<__nv_bfloat162*>(&v.w);
   const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
-  return fmaxf(__low2float(m), __high2float(m));
+  const __nv_bfloat16 mm = __hmax(__low2bfloat16(m), __high2bfloat16(m));
+  return static_cast<uint32_t>(__bfloat16_as_ushort(mm));
 }
 
 __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __restrict__ logits,
@@ -112,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
                                                           float* __restrict__ vals,
                                                           int32_t* __restrict__ idx,
                                                           uint32_t* __restrict__ err) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   TopkSmem& s = *reinterpret_cast<TopkSmem*>(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
@@ -130,7 +141,10 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
   if (tid < kTopK) s.top[tid] = 0ull;
   if (tid == 0) {
     s.count = 0;
+    s.count0 = 0;
+    s.overflow = 0;
     s.thr_key = 0ull;
+    s.init_thr = 0ull;
     for (int i = 0; i < kStages; ++i) mbar_init(&s.full_bar[i], 1);
     fence_mbar_init();
   }
@@ -158,21 +172,61 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
     }
     const int64_t e0 = static_cast<int64_t>(c) * kStageElems;
     const int chunk_elems = static_cast<int>(imin64(kStageElems, n_vec_elems - e0));
-    const uint64_t thr = s.thr_key;
-    // a threshold below every real value (empty / NaN) disables the fast reject
-    const bool exact_only = (thr >> 48) == 0ull;
-    const float thr_val = key_value(thr);
+    const uint32_t id_base = static_cast<uint32_t>(seg_begin + e0);
     const uint4* sv = reinterpret_cast<const uint4*>(s.stage[st]);
+    uint4 v[kVecPerThread];
+    uint32_t vmax[kVecPerThread];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kVecPerThread; ++h) {
       const int vi = tid + h * kThreads;
-      if (vi * 8 < chunk_elems) {
-        const uint4 v = sv[vi];
-        if (exact_only || vec_max(v) >= thr_val)
-          scan_vector(s, v, static_cast<uint32_t>(seg_begin + e0 + vi * 8), thr);
-      }
+      v[h] = (vi * 8 < chunk_elems) ? sv[vi] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+      vmax[h] = vec_max_bits(v[h]);
+    }
+    uint64_t thr = s.thr_key;
+    if ((thr >> 48) == 0ull) {
+      // Threshold still empty: a lower bound for this CTA's 16th best is the
+      // 16th largest of any warp's 32 per-thread maxima (16 distinct elements
+      // reach it).  Take the largest such bound over the warps.
+      // Threads without data contribute the empty key 0.
+      uint32_t tmax = 0;
+#pragma unroll
+      for (int h = 0; h < kVecPerThread; ++h)
+        if ((tid + h * kThreads) * 8 < chunk_elems) tmax = max(tmax, bf16_order(vmax[h]));
+      const uint64_t sorted = warp_sort_desc(static_cast<uint64_t>(tmax) << 48, lane);
+      if (lane == kTopK - 1) atomicMax(&s.init_thr, static_cast<unsigned long long>(sorted));
+      if (tid == 0) s.count0 = s.count;
+      __syncthreads();
+      thr = s.init_thr;
+      __syncthreads();
+      if (tid == 0) s.init_thr = 0ull;
+    } else if (tid == 0) {
+      s.count0 = s.count;
+    }
+    // elements equal to the bound keep qualifying (its id field is 0)
+    const bool exact_only = (thr >> 48) == 0ull;
+    const uint32_t thr_ord = static_cast<uint32_t>(thr >> 48);
+#pragma unroll
+    for (int h = 0; h < kVecPerThread; ++h) {
+      const int vi = tid + h * kThreads;
+      if (vi * 8 < chunk_elems && (exact_only || bf16_order(vmax[h]) >= thr_ord))
+        scan_vector(s, v[h], id_base + vi * 8, thr);
     }
     __syncthreads();   // stage consumed, all pushes visible
+    if (s.overflow) {
+      // Roll the chunk back (drop what it pushed), then rescan it in slices of
+      // 512 logits with a fold after each slice, so no slice can overflow.
+      const int n0 = s.count0;
+      __syncthreads();
+      fold_candidates(s, n0, warp, lane);
+      if (tid == 0) s.overflow = 0;
+      const int nvec = chunk_elems / 8;
+      for (int sl = 0; sl < nvec; sl += kRescanVecs) {
+        const uint64_t t2 = s.thr_key;
+        if (tid < kRescanVecs && sl + tid < nvec) scan_vector(s, sv[sl + tid], id_base + (sl + tid) * 8, t2);
+        __syncthreads();
+        fold_candidates(s, s.count, warp, lane);
+      }
+    }
     if (tid == 0 && c + kStages < n_chunks) {
       const int64_t e1 = static_cast<int64_t>(c + kStages) * kStageElems;
       const uint32_t bytes = static_cast<uint32_t>(imin64(kStageElems, n_vec_elems - e1) * 2);
@@ -180,11 +234,7 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
       bulk_g2s(s.stage[st], seg + e1, bytes, &s.full_bar[st], policy);
     }
     const int n = s.count;
-    if (n > kCompactAt) {
-      fold_candidates(s, n, warp, lane);
-      if (tid == 0) s.count = 0;
-      __syncthreads();
-    }
+    if (n > kCompactAt) fold_candidates(s, n, warp, lane);
   }
 
   if (aborted_at >= 0) {

@@ -71,6 +71,7 @@ struct VerifySmem {
   double candr[kTopK];        // residual weight of each candidate (unnormalized)
   float row_max;
   double row_z;
+  double cand_z;
   int skip;
   int token;
 };
@@ -96,13 +97,36 @@ __global__ void verify_init_kernel(int32_t* first_reject, int64_t B, int64_t L) 
   if (b < B) first_reject[b] = static_cast<int32_t>(L);
 }
 
+// True once an earlier position of the sequence is known to reject, i.e. row t
+// can no longer matter (first_reject only ever decreases).
+__device__ __forceinline__ bool row_irrelevant(const int32_t* first_reject, int64_t t) {
+  return t > *reinterpret_cast<const volatile int32_t*>(first_reject);
+}
+
+// Each warp polls first_reject every kPoll outer iterations and stops streaming
+// when the row has become irrelevant; its partial result is then garbage, which
+// is harmless because nothing derived from an irrelevant row is written.
+constexpr int kPoll = 2;
+
+__device__ __forceinline__ bool warp_should_stop(const int32_t* first_reject, int64_t t, int it) {
+  if ((it % kPoll) != kPoll - 1) return false;
+  int stop = 0;
+  if ((threadIdx.x & 31) == 0) stop = row_irrelevant(first_reject, t) ? 1 : 0;
+  return __shfl_sync(0xFFFFFFFFu, stop, 0) != 0;
+}
+
 // Arg-max of one row: lowest id among the largest values (NaN below -inf).
-__device__ int32_t row_argmax(VerifySmem& s, const uint16_t* row, int64_t V) {
+__device__ int32_t row_argmax(VerifySmem& s, const uint16_t* row, int64_t V, const int32_t* first_reject,
+                              int64_t t) {
   const int64_t nvec = V >> 3;
   const uint4* rv = reinterpret_cast<const uint4*>(row);
   uint64_t best = 0ull;   // (order << 32) | ~id
   int64_t i = threadIdx.x;
-  for (; i + 3 * kVThreads < nvec; i += 4 * kVThreads) {
+  for (int it = 0; i + 3 * kVThreads < nvec; i += 4 * kVThreads, ++it) {
+    if (warp_should_stop(first_reject, t, it)) {
+      i = nvec;
+      break;
+    }
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + u * kVThreads);
@@ -137,29 +161,42 @@ __device__ int32_t row_argmax(VerifySmem& s, const uint16_t* row, int64_t V) {
 
 // Softmax statistics of one row at inverse-temperature c = log2(e) / T:
 // row_max = max_v l_v, row_z = sum_v 2^((l_v - row_max) c).
-__device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V, float c) {
+__device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V, float c,
+                                  const int32_t* first_reject, int64_t t) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nvec = V >> 3;
   const uint4* rv = reinterpret_cast<const uint4*>(row);
   // Per thread: running max m and sum acc of 2^((l - m) c); each 8-element
-  // vector is summed in fp32 and added in fp64, so the row sum keeps ~1e-7
-  // relative accuracy.
+  // vector is summed in fp32 and added with Kahan compensation (fp64 is slow on
+  // this part), so the row sum keeps ~1e-7 relative accuracy.
   float m = -INFINITY;
-  double acc = 0.0;
+  float acc = 0.0f, comp = 0.0f;
+  auto add = [&](float x) {
+    const float y = x - comp;
+    const float t2 = acc + y;
+    comp = (t2 - acc) - y;
+    acc = t2;
+  };
   auto absorb = [&](const uint4& v) {
     const float vm = bf16_bits_to_float(vec_max_bits(v));
     if (vm > m) {
-      acc *= static_cast<double>(fast_exp2((m - vm) * c));
+      const float r = fast_exp2((m - vm) * c);
+      acc *= r;
+      comp *= r;
       m = vm;
     }
     const float mc = m * c;
     float vs = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) vs += fast_exp2(fmaf(bf16_bits_to_float(lane_bits(v, k)), c, -mc));
-    acc += static_cast<double>(vs);
+    add(vs);
   };
   int64_t i = threadIdx.x;
-  for (; i + 3 * kVThreads < nvec; i += 4 * kVThreads) {
+  for (int it = 0; i + 3 * kVThreads < nvec; i += 4 * kVThreads, ++it) {
+    if (warp_should_stop(first_reject, t, it)) {
+      i = nvec;
+      break;
+    }
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + u * kVThreads);
@@ -170,10 +207,12 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   for (int64_t e = nvec * 8 + threadIdx.x; e < V; e += kVThreads) {
     const float x = bf16_bits_to_float(row[e]);
     if (x > m) {
-      acc *= static_cast<double>(fast_exp2((m - x) * c));
+      const float r = fast_exp2((m - x) * c);
+      acc *= r;
+      comp *= r;
       m = x;
     }
-    acc += static_cast<double>(fast_exp2((x - m) * c));
+    add(fast_exp2((x - m) * c));
   }
   // combine (m, acc) over the block; the sum is carried in fp64
   float wm = m;
@@ -184,7 +223,9 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   float M = s.m[0];
 #pragma unroll
   for (int w = 1; w < kVWarps; ++w) M = fmaxf(M, s.m[w]);
-  double z = (m == -INFINITY) ? 0.0 : acc * static_cast<double>(fast_exp2((m - M) * c));
+  double z = (m == -INFINITY) ? 0.0
+                              : (static_cast<double>(acc) - static_cast<double>(comp)) *
+                                    static_cast<double>(fast_exp2((m - M) * c));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
   if (lane == 0) s.z[warp] = z;
@@ -198,55 +239,122 @@ __device__ void row_softmax_stats(VerifySmem& s, const uint16_t* row, int64_t V,
   __syncthreads();
 }
 
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
 // Inverse-CDF draw in id order over weights w_v = 2^((l_v - M) c), except that the
 // n_cand candidate ids in s.cand use the fp64 weights s.candr.  target_u in [0, 1).
+// Two levels, all loads coalesced: the row is cut into kVThreads contiguous
+// tiles of `per` elements; each warp sums 32 tiles (lanes read consecutive
+// 16-byte vectors, fp64 warp sum), candidates are corrected with shared-memory
+// atomics, thread 0 forms the tile prefix and picks the tile holding the target
+// mass, and warp 0 scans that tile 256 elements at a time (fp64 warp scan).
 __device__ int32_t row_draw(VerifySmem& s, const uint16_t* row, int64_t V, float c, int n_cand,
                             double target_u) {
-  const int tid = threadIdx.x;
-  const float M = s.row_max, mc = M * c;
-  const int64_t per = (V + kVThreads - 1) / kVThreads;   // contiguous elements per thread
-  const int64_t v0 = tid * per, v1 = (v0 + per < V) ? v0 + per : V;
-  double part = 0.0;
-  for (int64_t v = v0; v < v1; ++v) part += static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(row[v]), c, -mc)));
-  for (int j = 0; j < n_cand; ++j) {
-    const int64_t cv = s.cand[j];
-    if (cv >= v0 && cv < v1)
-      part += s.candr[j] - static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(row[cv]), c, -mc)));
-  }
-  part = part > 0.0 ? part : 0.0;
-  // exclusive scan of the per-thread masses in thread (= id) order
-  s.scan[tid] = part;
-  __syncthreads();
-  if (tid == 0) {
-    double run = 0.0;
-    for (int i = 0; i < kVThreads; ++i) {
-      const double p = s.scan[i];
-      s.scan[i] = run;
-      run += p;
-    }
-    s.row_z = run;   // total residual mass (row_z is no longer needed)
-    s.token = -1;
-  }
-  __syncthreads();
-  const double total = s.row_z;
-  const double target = target_u * total;
-  const double lo = s.scan[tid];
-  const double hi = (tid + 1 < kVThreads) ? s.scan[tid + 1] : total;
-  if (lo <= target && target < hi && v1 > v0) {
-    double run = lo;
-    int32_t pick = -1, last_pos = -1;
-    for (int64_t v = v0; v < v1; ++v) {
-      double w = static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(row[v]), c, -mc)));
-      for (int j = 0; j < n_cand; ++j)
-        if (s.cand[j] == v) w = s.candr[j];
-      if (w > 0.0) last_pos = static_cast<int32_t>(v);
-      run += w;
-      if (target < run) {
-        pick = static_cast<int32_t>(v);
-        break;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float mc = s.row_max * c;
+  const int64_t per = (((V + kVThreads - 1) / kVThreads) + 7) & ~int64_t(7);
+  auto weight = [&](int64_t v) -> double {
+    return static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(row[v]), c, -mc)));
+  };
+  for (int j = warp * 32; j < warp * 32 + 32; ++j) {
+    const int64_t v0 = j * per, v1 = (v0 + per < V) ? v0 + per : V;
+    double part = 0.0;
+    for (int64_t v = v0 + lane * 8; v < v1; v += 256) {
+      if (v + 8 <= v1) {
+        const uint4 x = *reinterpret_cast<const uint4*>(row + v);
+        float vs = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) vs += fast_exp2(fmaf(bf16_bits_to_float(lane_bits(x, k)), c, -mc));
+        part += static_cast<double>(vs);
+      } else {
+        for (int64_t e = v; e < v1; ++e) part += weight(e);
       }
     }
-    s.token = pick >= 0 ? pick : (last_pos >= 0 ? last_pos : static_cast<int32_t>(v0));
+    part = warp_sum_f64(part);
+    if (lane == 0) s.scan[j] = part;
+  }
+  __syncthreads();
+  if (tid < n_cand) atomicAdd(&s.scan[s.cand[tid] / per], s.candr[tid] - weight(s.cand[tid]));
+  __syncthreads();
+  if (tid == 0) {
+    double run = 0.0, target = 0.0;
+    int pick = -1;
+    double total = 0.0;
+    for (int j = 0; j < kVThreads; ++j) total += (s.scan[j] > 0.0 ? s.scan[j] : 0.0);
+    target = target_u * total;
+    for (int j = 0; j < kVThreads; ++j) {
+      const double pj = s.scan[j] > 0.0 ? s.scan[j] : 0.0;
+      if (pj > 0.0) {
+        if (target < run + pj || pick < 0) {
+          pick = j;
+          s.row_z = run;            // mass before the picked tile
+        }
+        if (target < run + pj) break;
+      }
+      run += pj;
+    }
+    s.token = pick;
+    s.cand_z = target;
+  }
+  __syncthreads();
+  const int tile = s.token;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t found = -1, last_pos = -1;
+    if (tile >= 0) {
+      const double target = s.cand_z;
+      double base = s.row_z;
+      const int64_t v0 = tile * per, v1 = (v0 + per < V) ? v0 + per : V;
+      for (int64_t cbase = v0; cbase < v1 && found < 0; cbase += 256) {
+        const int64_t v = cbase + lane * 8;
+        double w[8];
+        double mine = 0.0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          w[k] = 0.0;
+          if (v + k < v1) {
+            w[k] = weight(v + k);
+            for (int j = 0; j < n_cand; ++j)
+              if (s.cand[j] == v + k) w[k] = s.candr[j];
+          }
+          mine += w[k];
+        }
+        // inclusive warp scan of the lane masses
+        double incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double chunk = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, target < base + incl);
+        int lp = -1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (w[k] > 0.0) lp = static_cast<int>(v + k);
+        const unsigned has = __ballot_sync(0xFFFFFFFFu, lp >= 0);
+        if (has) last_pos = __shfl_sync(0xFFFFFFFFu, lp, 31 - __clz(has));
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          int32_t pick = -1;
+          if (lane == src) {
+            double run = base + incl - mine;
+            for (int k = 0; k < 8 && pick < 0; ++k) {
+              run += w[k];
+              if (target < run && w[k] > 0.0) pick = static_cast<int32_t>(v + k);
+            }
+            if (pick < 0) pick = lp;
+          }
+          found = __shfl_sync(0xFFFFFFFFu, pick, src);
+        }
+        base += chunk;
+      }
+    }
+    if (lane == 0) s.token = found >= 0 ? found : (last_pos >= 0 ? last_pos : 0);
   }
   __syncthreads();
   return s.token;
@@ -266,15 +374,18 @@ __global__ void __launch_bounds__(kVThreads)
   if (s.skip) return;
   const uint16_t* row = target + (b * (L + 1) + t) * ld;
   if (temperature <= 0.0f) {
-    const int32_t a = row_argmax(s, row, V);
-    if (threadIdx.x == 0) {
+    const int32_t a = row_argmax(s, row, V, first_reject + b, t);
+    if (threadIdx.x == 0 && !row_irrelevant(first_reject + b, t)) {
       out_tok[b * (L + 1) + t] = a;
       if (t < L && draft_tok[b * L + t] != a) atomicMin(first_reject + b, static_cast<int32_t>(t));
     }
     return;
   }
   const float c = kLog2e / temperature;
-  row_softmax_stats(s, row, V, c);
+  row_softmax_stats(s, row, V, c, first_reject + b, t);
+  if (threadIdx.x == 0) s.skip = row_irrelevant(first_reject + b, t) ? 1 : 0;
+  __syncthreads();
+  if (s.skip) return;
   if (t == L) {
     const double u = philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(L), 2, offset);
     const int32_t tok = row_draw(s, row, V, c, 0, u);

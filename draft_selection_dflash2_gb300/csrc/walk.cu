@@ -8,8 +8,14 @@
 // 16-byte loads, so the L dependent steps run out of shared memory instead of
 // paying a global-memory round trip each.  Lane j (j < 16) owns successor slot j.
 //   greedy : shuffle arg-max over (value, lowest slot).
-//   sampled: w_j = exp((S_j - max) / T) in fp64; lane 0 sums Z and the CDF in
-//            slot order and draws with the Philox uniform of (b, t, stream 0).
+//   sampled: everything in fp32 (the draw is an integer decided by floating
+//            point): c = log2(e) / T, w_j = exp2_neg((S_j - max) * c), Z and the
+//            CDF summed in slot order, u the Philox uniform of (b, t, stream 0)
+//            (24 bits, exact in fp32), slot = smallest j with u Z < CDF_j,
+//            q_j = w_j / Z.  exp2_neg follows Cody and Waite's reduction with a
+//            degree-7 Taylor polynomial, and every step is a correctly rounded
+//            IEEE operation (explicit _rn intrinsics, no contraction), so the
+//            draw is reproducible by any implementation of the same steps.
 #include "common.cuh"
 #include "launch.h"
 #include "philox.cuh"
@@ -17,12 +23,31 @@
 namespace dflash2 {
 namespace {
 
+// 2^x for x <= 0 in fp32: x = n + f, n = rint(x), f in [-1/2, 1/2]; 2^f by the
+// degree-7 Taylor polynomial of e^(f ln 2) (coefficients (ln 2)^k / k! rounded
+// to fp32) in Horner form with fused multiply-adds; times 2^n (exact scaling,
+// correctly rounded when the result is subnormal); 0 below -126 and for NaN.
+__device__ __forceinline__ float exp2_neg(float x) {
+  if (!(x >= -126.0f)) return 0.0f;
+  const float n = rintf(x);
+  const float f = __fsub_rn(x, n);
+  float p = 1.525273365e-05f;
+  p = __fmaf_rn(p, f, 1.540352969e-04f);
+  p = __fmaf_rn(p, f, 1.333355787e-03f);
+  p = __fmaf_rn(p, f, 9.618128650e-03f);
+  p = __fmaf_rn(p, f, 5.550410971e-02f);
+  p = __fmaf_rn(p, f, 2.402265072e-01f);
+  p = __fmaf_rn(p, f, 6.931471825e-01f);
+  p = __fmaf_rn(p, f, 1.0f);
+  return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
+}
+
 constexpr int kWalkWarps = 2;            // sequences per CTA (2 x 64 KB at L = 64)
 constexpr int kMaxWalkL = 64;
 
 __global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand_idx, int64_t B,
-                int64_t L, double temperature, uint64_t seed, uint64_t offset,
+                int64_t L, float temperature, uint64_t seed, uint64_t offset,
                 int32_t* __restrict__ draft_tok, int32_t* __restrict__ draft_slot,
                 float* __restrict__ draft_q) {
   extern __shared__ __align__(16) float wsm[];
@@ -37,6 +62,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   __syncwarp();
 
   const int j = lane & (kTopK - 1);
+  const float cinv = temperature > 0.0f ? __fdiv_rn(1.44269504f, temperature) : 0.0f;
   int prev = 0;
   for (int64_t t = 0; t < L; ++t) {
     const float v = sb[(t * kTopK + prev) * kTopK + j];
@@ -54,36 +80,37 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     }
     int chosen;
     const int64_t q_at = (b * L + t) * kTopK + j;
-    if (temperature <= 0.0) {
+    if (temperature <= 0.0f) {
       chosen = bj;
       if (draft_q && lane < kTopK) draft_q[q_at] = (j == chosen) ? 1.0f : 0.0f;
     } else {
-      const double w = exp((static_cast<double>(v) - static_cast<double>(bv)) / temperature);
+      const float w = exp2_neg(__fmul_rn(__fsub_rn(v, bv), cinv));
       // Every lane gathers the 16 weights and repeats the (identical) slot-order
       // sums, so no broadcast is needed afterwards.
-      double wj[kTopK];
-#pragma unroll
-      for (int i = 0; i < kTopK; ++i) wj[i] = __shfl_sync(0xFFFFFFFFu, w, i);
-      double Z = 0.0;
-#pragma unroll
-      for (int i = 0; i < kTopK; ++i) Z += wj[i];
-      const double target =
-          philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset) * Z;
-      int pick = -1;
-      double run = 0.0;
+      float cdf[kTopK];
+      float Z = 0.0f;
 #pragma unroll
       for (int i = 0; i < kTopK; ++i) {
-        run += wj[i];
-        if (pick < 0 && target < run) pick = i;
+        Z = __fadd_rn(Z, __shfl_sync(0xFFFFFFFFu, w, i));
+        cdf[i] = Z;
       }
-      if (pick < 0)
+      const float u = static_cast<float>(
+          philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset));
+      const float target = __fmul_rn(u, Z);
+      int pick = -1;
+#pragma unroll
+      for (int i = kTopK - 1; i >= 0; --i)
+        if (target < cdf[i]) pick = i;
+      if (pick < 0) {
+        // u Z below every partial sum cannot fail for u < 1; keep the last positive weight
         for (int i = kTopK - 1; i >= 0; --i)
-          if (wj[i] > 0.0) {
+          if (cdf[i] > (i > 0 ? cdf[i - 1] : 0.0f)) {
             pick = i;
             break;
           }
+      }
       chosen = pick;
-      if (draft_q && lane < kTopK) draft_q[q_at] = static_cast<float>(w / Z);
+      if (draft_q && lane < kTopK) draft_q[q_at] = __fdiv_rn(w, Z);
     }
     if (lane == 0) {
       draft_slot[b * L + t] = chosen;
@@ -107,7 +134,7 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>((B + kWalkWarps - 1) / kWalkWarps);
-  walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, static_cast<double>(temperature),
+  walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, temperature,
                                                        seed, offset, draft_tok, draft_slot, draft_q);
   return cudaGetLastError();
 }

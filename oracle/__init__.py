@@ -35,6 +35,8 @@ def _load():
         lib.oracle_philox4x32_10.restype = None
         lib.oracle_uniform24.argtypes = [U64, U64, U64, ctypes.c_uint32, U64]
         lib.oracle_uniform24.restype = D
+        lib.oracle_exp2_neg.argtypes = [ctypes.c_float]
+        lib.oracle_exp2_neg.restype = ctypes.c_float
         lib.oracle_topk.argtypes = [P, I64, I64, I64, I, P, P, I]
         lib.oracle_topk.restype = None
         lib.oracle_gate.argtypes = [P, P, P, I64, I64, I64, P, I]
@@ -83,6 +85,11 @@ def philox4x32_10(ctr, key):
 
 def uniform24(seed, b, t, stream, offset=0):
     return float(_load().oracle_uniform24(seed, b, t, stream, offset))
+
+
+def exp2_neg(x: float) -> float:
+    """The walk's fp32 2^x (x <= 0): Cody-Waite reduction + degree-7 Taylor polynomial."""
+    return float(_load().oracle_exp2_neg(float(x)))
 
 
 def topk(logits_bits, k=16, V=None, nthreads=None):

@@ -25,6 +25,11 @@
 //   R4  greedy walk = myopic best successor at every step, lowest slot on ties.
 //   R5  sampled walk = softmax(S/T) over the 16 successors of the chosen
 //       predecessor, inverse CDF in slot order with a Philox4x32-10 uniform.
+//       The draw is an integer decided by floating point, so it is taken in
+//       the kernel's precision (fp32) with 2^x evaluated by a named method
+//       (Cody-Waite reduction + degree-7 Taylor polynomial, exp2_neg below):
+//       every step is a correctly rounded IEEE fp32 operation, so any
+//       implementation of the same steps draws the same slot.
 //   R6  conv correction [c0; c1] = W_c h_t (+ b_c), linear, no activation;
 //       rows [0, d/16) give c0, rows [d/16, 2d/16) give c1; channel ch belongs
 //       to group ch/16; h defaults to the conv input x; no residual.
@@ -106,6 +111,27 @@ double uniform24(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, uint64_
   return static_cast<double>(out[0] >> 8) * (1.0 / 16777216.0);
 }
 
+// 2^x for x <= 0 in fp32 (reading R5).  Cody and Waite's range reduction
+// (Software Manual for the Elementary Functions, 1980): x = n + f with
+// n = rint(x) and f in [-1/2, 1/2]; 2^f = e^(f ln 2) by the degree-7 Taylor
+// polynomial, coefficients (ln 2)^k / k! rounded to fp32, in Horner form with
+// fused multiply-adds; then an exact scaling by 2^n.  0 below -126 (and for NaN).
+// Truncation error (f ln 2)^8 / 8! < 4e-10, below half an fp32 ulp.
+float exp2_neg(float x) {
+  if (!(x >= -126.0f)) return 0.0f;
+  const float n = std::nearbyint(x);
+  const float f = x - n;
+  float p = 1.525273365e-05f;            // (ln 2)^7 / 7!
+  p = std::fma(p, f, 1.540352969e-04f);  // (ln 2)^6 / 6!
+  p = std::fma(p, f, 1.333355787e-03f);  // (ln 2)^5 / 5!
+  p = std::fma(p, f, 9.618128650e-03f);  // (ln 2)^4 / 4!
+  p = std::fma(p, f, 5.550410971e-02f);  // (ln 2)^3 / 3!
+  p = std::fma(p, f, 2.402265072e-01f);  // (ln 2)^2 / 2!
+  p = std::fma(p, f, 6.931471825e-01f);  // ln 2
+  p = std::fma(p, f, 1.0f);
+  return std::ldexp(p, static_cast<int>(n));
+}
+
 // Reading R1: does (va, ia) come strictly before (vb, ib) in top-k order?
 bool ranks_before(double va, int64_t ia, double vb, int64_t ib) {
   const bool na = std::isnan(va), nb = std::isnan(vb);
@@ -135,6 +161,8 @@ void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* ou
 double oracle_uniform24(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, uint64_t offset) {
   return uniform24(seed, b, t, stream, offset);
 }
+
+float oracle_exp2_neg(float x) { return exp2_neg(x); }
 
 // ---------------------------------------------------------------------------
 // Stage 1: per-position top-k candidates.
@@ -225,9 +253,10 @@ int oracle_pair_scores(const int32_t* cand_idx, const float* cand_val,
 //   row(t) = 0 for t = 0 (all rows are equal there), else slot(t - 1).
 //   temperature <= 0: slot(t) = lowest j maximising S[b, t, row, j] (R4);
 //                     q[b, t, :] = one-hot at slot(t).
-//   temperature  > 0: w_j = exp((S_j - max S) / T) in double, Z = w_0 + ... + w_15
-//                     summed in slot order, u = uniform24(seed, b, t, 0, offset),
-//                     slot(t) = smallest j with u * Z < w_0 + ... + w_j (R5);
+//   temperature  > 0 (R5, all in fp32): c = log2(e) / T,
+//                     w_j = exp2_neg((S_j - max S) * c), Z = w_0 + ... + w_15 summed
+//                     in slot order, u = uniform24(seed, b, t, 0, offset) (exact in
+//                     fp32), slot(t) = smallest j with u * Z < w_0 + ... + w_j;
 //                     q[b, t, j] = w_j / Z.
 // S: [B, L, K, K] fp32 (the walk reads scores at the precision they are stored);
 // outputs draft_tok, draft_slot: [B, L]; q: [B, L, K] or null;
@@ -258,16 +287,17 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
         if (q)
           for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = (j == chosen) ? 1.0f : 0.0f;
       } else {
-        const double m = static_cast<double>(s[best]);
-        std::vector<double> w(static_cast<size_t>(K)), cdf(static_cast<size_t>(K));
-        double Z = 0.0;
+        const float m = s[best];
+        const float c = 1.44269504f / static_cast<float>(temperature);
+        float w[64], cdf[64];
+        float Z = 0.0f;
         for (int64_t j = 0; j < K; ++j) {
-          w[j] = std::exp((static_cast<double>(s[j]) - m) / temperature);
+          w[j] = exp2_neg((s[j] - m) * c);
           Z += w[j];
           cdf[j] = Z;
         }
-        const double u = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 0, offset);
-        const double target = u * Z;
+        const float u = static_cast<float>(uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 0, offset));
+        const float target = u * Z;
         chosen = -1;
         for (int64_t j = 0; j < K; ++j)
           if (target < cdf[j]) {
@@ -276,15 +306,15 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
           }
         if (chosen < 0)
           for (int64_t j = K - 1; j >= 0; --j)
-            if (w[j] > 0.0) {
+            if (w[j] > 0.0f) {
               chosen = j;
               break;
             }
-        double gap = cdf[chosen] - target;
-        if (chosen > 0) gap = std::min(gap, target - cdf[chosen - 1]);
+        double gap = static_cast<double>(cdf[chosen]) - target;
+        if (chosen > 0) gap = std::min(gap, static_cast<double>(target) - cdf[chosen - 1]);
         step_margin = gap / Z;
         if (q)
-          for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = static_cast<float>(w[j] / Z);
+          for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = w[j] / Z;
       }
       draft_slot[b * L + t] = static_cast<int32_t>(chosen);
       draft_tok[b * L + t] = cand_idx[(b * L + t) * K + chosen];

@@ -293,7 +293,8 @@ def test_walk_sampling_distribution_and_q():
             assert q[0, 0, i] / q[0, 0, j] == pytest.approx(math.exp((row[i] - row[j]) / T), rel=1e-6)
     assert q[0, 0].sum() == pytest.approx(1.0, abs=1e-6)
     counts = np.bincount(slot[:, 0], minlength=K)
-    assert stats.chisquare(counts, q[0, 0].astype(np.float64) / q[0, 0].sum() * n).pvalue > 1e-4
+    q64 = q[0, 0].astype(np.float64)
+    assert stats.chisquare(counts, q64 / q64.sum() * n).pvalue > 1e-4
 
 
 def test_walk_low_temperature_matches_greedy():
@@ -570,3 +571,31 @@ def test_verify_philox_streams_are_pinned():
             assert acc[b] == 1
             assert out[b, 0] == others[int(15 * oracle.uniform24(seed, b, 0, 2, off))]
     assert 5 < n_acc < 60
+
+
+# ---------------------------------------------------------------------------
+# the walk's fp32 2^x
+# ---------------------------------------------------------------------------
+
+
+def test_exp2_neg_exact_points():
+    assert oracle.exp2_neg(0.0) == 1.0
+    assert oracle.exp2_neg(-1.0) == 0.5
+    assert oracle.exp2_neg(-126.0) == 2.0**-126
+    assert oracle.exp2_neg(-127.0) == 0.0
+    assert oracle.exp2_neg(float("-inf")) == 0.0
+    assert oracle.exp2_neg(float("nan")) == 0.0
+    for n in range(0, 126):
+        assert oracle.exp2_neg(-float(n)) == 2.0 ** -n
+
+
+def test_exp2_neg_within_one_ulp_of_exact():
+    # against the exact value (math.exp2 in double), over [-126, 0] including
+    # the rint half-way points; one fp32 ulp relative = 2^-23
+    xs = np.concatenate([np.linspace(-126.0, 0.0, 200001, dtype=np.float32),
+                         np.arange(-125.5, 0.0, 1.0, dtype=np.float32),
+                         -np.logspace(-8, 0, 2001).astype(np.float32)])
+    for x in xs:
+        got = oracle.exp2_neg(float(x))
+        ref = math.exp2(float(x))
+        assert abs(got - ref) <= 2.0**-23 * ref, (float(x), got, ref)
