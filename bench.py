@@ -322,6 +322,8 @@ def run_gpu(args):
         line["sweep"] = run_sweep(torch, api, h, w, cyc, dev, pk)
     if rank == 0 and args.e2e:
         line["e2e"] = run_e2e(torch, api, h, w, cyc, dev, args)
+    if rank == 0 and args.lmhead:
+        line["lmhead"] = run_lmhead(torch, api, h, dev, pk)
     if rank == 0 and args.cpu_baseline and world == 1:
         line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=64)
     if rank == 0:
@@ -375,6 +377,46 @@ def run_sweep(torch, api, h, w, cyc, dev, pk):
                     "topk_frac_hbm": round(bytes_topk(nb) / (med["topk"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                     "walk_us": round(med["walk"] * 1e3, 2)})
     return out
+
+
+def run_lmhead(torch, api, h, dev, pk, M=1024):
+    """Fused LM head + top-16 on hidden [1024, 5120] x W [151936, 5120] (bf16,
+    N(0,1) and N(0,0.02), drawn on the device with a seeded torch generator),
+    against the unfused library path: cuBLAS bf16 GEMM writing the logits, then
+    dflash2_topk over them (timing comparison only)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    hidden = torch.randn((M, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    W = (torch.randn((V, D), generator=g, device=dev, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    ws = torch.empty(max(api.lmhead_topk_workspace(h, M, V, D), 256), dtype=torch.uint8, device=dev)
+    vals = torch.empty((M, K), dtype=torch.float32, device=dev)
+    idx = torch.empty((M, K), dtype=torch.int32, device=dev)
+    flops = 2.0 * M * V * D
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    fused_ms = timed(lambda: api.lmhead_topk(h, hidden, W, vals=vals, idx=idx, workspace=ws))
+    logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    unfused_ms = timed(lambda: (torch.matmul(hidden, W.t(), out=logits), api.topk(h, logits, vals=vals, idx=idx)))
+    tf = flops / (fused_ms * 1e-3) / 1e12
+    del logits, W, hidden
+    return {"workload": f"fused LM-head top-16 M={M} d={D} V={V}", "fused_ms": round(fused_ms, 4),
+            "unfused_cublas_plus_topk_ms": round(unfused_ms, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
+                         "peak_source": pk["source"] + " (bf16 burst, MEASURED_PEAKS.json)"}}
 
 
 def run_e2e(torch, api, h, w, cyc, dev, args):
@@ -491,6 +533,7 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-lmhead", dest="lmhead", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -32,7 +32,7 @@ SIGNATURES = {
     "dflash2_walk": (I32, [P, P, P, I64, I64, F32, U64, U64, P, P, P, P]),
     "dflash2_conv2tap": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, P, I32, P]),
     "dflash2_verify": (I32, [P, P, I64, P, P, P, P, I64, I64, I64, F32, U64, U64, P, P, P]),
-    "dflash2_lmhead_topk_workspace": (SZ, [I64, I64, I64]),
+    "dflash2_lmhead_topk_workspace": (SZ, [P, I64, I64, I64]),
     "dflash2_lmhead_topk": (I32, [P, P, P, I64, I64, I64, P, P, P, SZ, P]),
 }
 

@@ -176,8 +176,8 @@ def verify(h: Handle, target, draft_tok, draft_slot=None, draft_q=None, cand_idx
     return accept_len, out_tok
 
 
-def lmhead_topk_workspace(M: int, V: int, d: int) -> int:
-    return int(_lib.load().dflash2_lmhead_topk_workspace(M, V, d))
+def lmhead_topk_workspace(h: Handle, M: int, V: int, d: int) -> int:
+    return int(h._lib.dflash2_lmhead_topk_workspace(h.ptr, M, V, d))
 
 
 def lmhead_topk(h: Handle, hidden, W, vals=None, idx=None, workspace=None, stream=None):
@@ -187,7 +187,7 @@ def lmhead_topk(h: Handle, hidden, W, vals=None, idx=None, workspace=None, strea
     dev = hidden.device
     vals = torch.empty((M, K), dtype=torch.float32, device=dev) if vals is None else vals
     idx = torch.empty((M, K), dtype=torch.int32, device=dev) if idx is None else idx
-    need = lmhead_topk_workspace(M, V, d)
+    need = lmhead_topk_workspace(h, M, V, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(h._lib.dflash2_lmhead_topk(h.ptr, _ptr(hidden), _ptr(W), M, V, d, _ptr(vals), _ptr(idx),

@@ -187,9 +187,9 @@ int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const 
                                          h->num_sms, as_stream(stream)));
 }
 
-size_t dflash2_lmhead_topk_workspace(int64_t M, int64_t V, int64_t d) {
-  if (M <= 0 || V <= 0 || d <= 0) return 0;
-  return dflash2::lmhead_workspace_bytes(M, V, d);
+size_t dflash2_lmhead_topk_workspace(const dflash2_handle* h, int64_t M, int64_t V, int64_t d) {
+  if (bad_handle(h) || M <= 0 || V <= 0 || d <= 0) return 0;
+  return dflash2::lmhead_workspace_bytes(M, V, d, h->num_sms);
 }
 
 int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
@@ -202,7 +202,7 @@ int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(vals, 4) || !aligned(idx, 4) ||
       (workspace && !aligned(workspace, 256)))
     return DFLASH2_ERR_MISALIGNED;
-  if (ws_bytes < dflash2::lmhead_workspace_bytes(M, V, d) || workspace == nullptr)
+  if (workspace == nullptr || ws_bytes < dflash2::lmhead_workspace_bytes(M, V, d, h->num_sms))
     return DFLASH2_ERR_WORKSPACE;
   return launched(dflash2::launch_lmhead_topk(hidden, W, M, V, d, vals, idx, workspace, h->num_sms,
                                               h->err, as_stream(stream)));

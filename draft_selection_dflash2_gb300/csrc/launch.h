@@ -32,7 +32,7 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
                           uint64_t offset, int32_t* accept_len, int32_t* out_tok, uint32_t* err,
                           int num_sms, cudaStream_t stream);
 
-size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d);
+size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms);
 cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,
                                int64_t d, float* vals, int32_t* idx, void* workspace,
                                int num_sms, uint32_t* err, cudaStream_t stream);

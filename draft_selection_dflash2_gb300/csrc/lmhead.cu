@@ -1,20 +1,311 @@
-// lmhead.cu -- fused LM head + top-16 (placeholder until the tensor-core kernel lands).
+// lmhead.cu -- fused LM head + top-16: logits = hidden W^T on the tensor cores,
+// reduced to each hidden row's 16 best (value, id) pairs on chip, so no logit
+// ever reaches global memory.  The head produces the drafter's own logits U_t
+// whose top 16 the path selector keeps ("DFlash 2: Keep Drafting Parallel",
+// "A Lightweight Path Selector").
+//
+// lmhead_kernel (persistent, one CTA per SM):
+//   CTA c owns hidden-row tile mt = c % m_tiles (128 rows) and a contiguous run
+//   of vocabulary tiles (256 ids each), so the m_tiles CTAs sharing a run read
+//   the same W tiles at about the same time and W streams from HBM once (the
+//   other reads hit L2).
+//   warp 0      TMA producer: 128 x 64 hidden tiles + 256 x 64 W tiles into a
+//               4-deep ring (48 KB per stage, 128-byte swizzle).
+//   warp 1      allocates 512 TMEM columns = two 128 x 256 fp32 accumulators;
+//               lane 0 issues 4 tcgen05.mma (128 x 256 x 16) per stage into the
+//               current buffer and commits it when the tile's K loop is done.
+//   warps 2..5  epilogue: each thread owns one hidden row (one TMEM lane) and
+//               keeps its running top-16 in registers; it reads the finished
+//               buffer 32 columns at a time (tcgen05.ld) and inserts the rare
+//               logits above its 16th best, then hands the buffer back, so
+//               the epilogue of tile i overlaps the MMAs of tile i + 1.
+//   At the end each thread writes its list as 16 order-preserving 64-bit keys
+//   (fp32 value, -id) to the workspace [M, n_runs, 16].
+// lmhead_merge_kernel: one warp per row folds the n_runs partial lists into the
+// final top-16 (value descending, lowest id on ties).
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace dflash2 {
+namespace {
 
-size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d) {
-  (void)M; (void)V; (void)d;
-  return 256;
+constexpr int kLmBN = 256;
+constexpr int kLmStages = 4;
+constexpr int kLmThreads = 192;
+constexpr int kLmABytes = 128 * kTileRowBytes;                 // 16 KB
+constexpr int kLmBBytes = kLmBN * kTileRowBytes;               // 32 KB
+constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
+constexpr uint32_t kLmTmemCols = 2 * kLmBN;                    // double-buffered accumulator
+constexpr uint32_t kLmIdesc = umma_idesc_bf16(128, kLmBN);
+
+struct LmSmem {
+  uint64_t full[kLmStages];
+  uint64_t empty[kLmStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem;
+  int abort_flag;
+};
+
+// Order-preserving 64-bit key of an fp32 logit and its id: larger key ranks
+// first (value descending, then id ascending); 0 is "empty".
+__device__ __forceinline__ uint64_t logit_key(float v, int32_t id) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;                       // -0 == +0
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(~static_cast<uint32_t>(id));
+}
+
+__device__ __forceinline__ float logit_key_value(uint64_t k) {
+  const uint32_t ord = static_cast<uint32_t>(k >> 32);
+  const uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+  return __uint_as_float(b);
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
+                  int64_t V, int d, int m_tiles, int n_tiles, int tiles_per_run, int n_runs,
+                  uint64_t* __restrict__ partial, uint32_t* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  LmSmem& s = *reinterpret_cast<LmSmem*>(ring + kLmStages * kLmStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x % m_tiles;
+  const int run = blockIdx.x / m_tiles;
+  const int nt0 = run * tiles_per_run;
+  const int nt1 = min(n_tiles, nt0 + tiles_per_run);
+  const int ntiles = max(0, nt1 - nt0);
+  const int nk = d / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kLmStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);       // one arrival per epilogue warp
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem, kLmTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_last();    // hidden rows: reused by every tile
+      // W tiles are read by the m_tiles CTAs sharing a run at slightly different
+      // times: normal priority keeps them in L2 until the last of those reads
+      uint64_t pol_b;
+      asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_b));
+      int it = 0, issued = 0;
+      for (int i = 0; i < ntiles && !*abort_flag; ++i) {
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % kLmStages;
+          if (it >= kLmStages && !mbar_wait_bounded(&s.empty[st], ((it / kLmStages) - 1) & 1, err)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* a_dst = ring + st * kLmStageBytes;
+          mbar_arrive_expect_tx(&s.full[st], kLmStageBytes);
+          tma_load_2d(a_dst, &tmA, kb * kBK, mt * 128, &s.full[st], pol_a);
+          tma_load_2d(a_dst + kLmABytes, &tmB, kb * kBK, (nt0 + i) * kLmBN, &s.full[st], pol_b);
+          issued = it + 1;
+        }
+      }
+      for (int j = issued - kLmStages > 0 ? issued - kLmStages : 0; j < issued; ++j)
+        mbar_wait_bounded(&s.full[j % kLmStages], (j / kLmStages) & 1, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait_bounded(&s.tempty[buf], ((i >> 1) - 1) & 1, err)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * kLmBN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % kLmStages;
+          if (!mbar_wait_bounded(&s.full[st], (it / kLmStages) & 1, err) || *abort_flag) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(ring + st * kLmStageBytes);
+          const uint32_t b_base = a_base + kLmABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_bf16(acc, umma_desc_sw128(a_base + k * 32), umma_desc_sw128(b_base + k * 32), kLmIdesc,
+                      (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&s.empty[st]);
+        }
+        umma_commit(&s.tfull[buf]);
+        if (!ok) break;
+      }
+    }
+  } else {
+    // epilogue: one hidden row per thread
+    const int q = warp & 3;
+    const int row = mt * 128 + q * 32 + lane;
+    const bool row_ok = row < M;
+    float val[kTopK];
+    int32_t ids[kTopK];
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) {
+      val[k] = -INFINITY;
+      ids[k] = 0x7FFFFFFF;
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      const int buf = i & 1;
+      if (!mbar_wait_bounded(&s.tfull[buf], (i >> 1) & 1, err) || *abort_flag) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int64_t id_base = static_cast<int64_t>(nt0 + i) * kLmBN;
+#pragma unroll 1
+      for (int c = 0; c < kLmBN / 32; ++c) {
+        float v[32];
+        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kLmBN + c * 32, v);
+        tmem_ld_wait();
+        const int64_t id0 = id_base + c * 32;
+        if (!row_ok) continue;
+        // the common case (nothing above the row's 16th best) costs one compare
+        // per logit; the sorted insertion stays a compact loop
+        float m = v[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) m = fmaxf(m, v[j]);
+        if (m > val[kTopK - 1]) {
+#pragma unroll 1
+          for (int j = 0; j < 32; ++j) {
+            const float x = v[j];
+            if (x > val[kTopK - 1] && id0 + j < V) {
+              // ids arrive in increasing order, so an equal value (larger id)
+              // never displaces an existing entry
+              float cv = x;
+              int32_t ci = static_cast<int32_t>(id0 + j);
+#pragma unroll
+              for (int k = 0; k < kTopK; ++k) {
+                const bool sw = cv > val[k];
+                const float tv = val[k];
+                const int32_t ti = ids[k];
+                val[k] = sw ? cv : tv;
+                ids[k] = sw ? ci : ti;
+                cv = sw ? tv : cv;
+                ci = sw ? ti : ci;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[buf]);
+    }
+    if (row_ok) {
+      uint64_t* dst = partial + (static_cast<int64_t>(row) * n_runs + run) * kTopK;
+#pragma unroll
+      for (int k = 0; k < kTopK; ++k) dst[k] = (ids[k] == 0x7FFFFFFF) ? 0ull : logit_key(val[k], ids[k]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      umma_commit(&s.drain);
+      mbar_wait_bounded(&s.drain, 0, err);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kLmTmemCols);
+  }
+}
+
+// One warp per row: the top-16 of the row's n_runs partial lists.
+__global__ void lmhead_merge_kernel(const uint64_t* __restrict__ partial, int M, int n_runs,
+                                    float* __restrict__ vals, int32_t* __restrict__ idx) {
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint64_t* src = partial + static_cast<int64_t>(row) * n_runs * kTopK;
+  const int n = n_runs * kTopK;
+  uint64_t top = 0ull;
+  for (int base = 0; base < n; base += 32) top = warp_merge_top16(top, base + lane < n ? src[base + lane] : 0ull, lane);
+  if (lane < kTopK) {
+    vals[static_cast<int64_t>(row) * kTopK + lane] = logit_key_value(top);
+    idx[static_cast<int64_t>(row) * kTopK + lane] = static_cast<int32_t>(~static_cast<uint32_t>(top));
+  }
+}
+
+struct LmPlan {
+  int m_tiles, n_tiles, n_runs, tiles_per_run, grid;
+};
+
+LmPlan lm_plan(int64_t M, int64_t V, int num_sms) {
+  LmPlan p;
+  p.m_tiles = static_cast<int>((M + 127) / 128);
+  p.n_tiles = static_cast<int>((V + kLmBN - 1) / kLmBN);
+  int runs = num_sms / p.m_tiles;
+  if (runs < 1) runs = 1;
+  if (runs > p.n_tiles) runs = p.n_tiles;
+  p.tiles_per_run = (p.n_tiles + runs - 1) / runs;
+  p.n_runs = (p.n_tiles + p.tiles_per_run - 1) / p.tiles_per_run;
+  p.grid = p.m_tiles * p.n_runs;
+  return p;
+}
+
+}  // namespace
+
+size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms) {
+  (void)d;
+  const LmPlan p = lm_plan(M, V, num_sms);
+  return static_cast<size_t>(M) * p.n_runs * kTopK * sizeof(uint64_t);
 }
 
 cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,
                                int64_t d, float* vals, int32_t* idx, void* workspace, int num_sms,
                                uint32_t* err, cudaStream_t stream) {
-  (void)hidden; (void)W; (void)M; (void)V; (void)d; (void)vals; (void)idx; (void)workspace;
-  (void)num_sms; (void)err; (void)stream;
-  return cudaErrorNotSupported;
+  if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const LmPlan p = lm_plan(M, V, num_sms);
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, kLmBN))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + kLmStages * kLmStageBytes + sizeof(LmSmem);
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  uint64_t* partial = static_cast<uint64_t*>(workspace);
+  lmhead_kernel<<<p.grid, kLmThreads, smem, stream>>>(ta, tb, static_cast<int>(M), V, static_cast<int>(d),
+                                                       p.m_tiles, p.n_tiles, p.tiles_per_run, p.n_runs, partial,
+                                                       err);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows_per_block = 8;
+  lmhead_merge_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,
+                        stream>>>(partial, static_cast<int>(M), p.n_runs, vals, idx);
+  return cudaGetLastError();
 }
 
 }  // namespace dflash2

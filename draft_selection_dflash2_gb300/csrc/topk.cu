@@ -5,17 +5,19 @@
 // Design (HBM-bound stream, 2 bytes per logit):
 //   * A row is split into `S` contiguous segments, one per CTA of an S-CTA
 //     thread-block cluster (S = 1 when there are enough rows to fill the GPU).
-//   * Each CTA streams its segment through a ring of shared-memory stages with
-//     1-D bulk TMA copies (cp.async.bulk, evict-first L2 policy), so global
-//     loads are 8 KB transactions issued by one thread.
-//   * Every thread scans 16 logits per stage.  A packed bf16x2 max over those
-//     16 against the CTA's running 16th-best value rejects almost every group
-//     in ~10 instructions; survivors are turned into exact 64-bit keys
-//     (value, -id) and appended to a shared candidate buffer.
-//   * When the buffer passes 64 entries (and at the end) the warps fold it into
-//     the running top-16 with warp-level bitonic merges and raise the threshold.
-//   * The S partial lists meet in distributed shared memory: CTA rank 0 reads
-//     them with ld.shared::cluster, merges and writes the row's output.
+//   * A producer warp streams the segment through a ring of 16 KB shared-memory
+//     stages with 1-D bulk TMA copies (cp.async.bulk, evict-first L2 policy);
+//     each stage is refilled as soon as the eight consumer warps have arrived
+//     on its "empty" mbarrier, so the ring never waits for a CTA barrier.
+//   * Each consumer warp owns 1/8 of every stage and keeps its own running
+//     top-16 (one key per lane), threshold and 64-entry candidate buffer: a
+//     packed bf16x2 max over each lane's 8 logits against the warp threshold
+//     rejects almost every vector; survivors become exact 64-bit keys
+//     (value, -id) appended with warp ballots, folded into the warp's top-16
+//     with bitonic merges whenever more than 32 are pending.
+//   * At the end the eight warp lists are merged, then the S CTA lists meet in
+//     distributed shared memory: CTA rank 0 reads them with ld.shared::cluster,
+//     merges and writes the row's output.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -26,86 +28,27 @@ namespace cg = cooperative_groups;
 namespace dflash2 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kStageBytes = 16384;                   // 8192 logits per stage
 constexpr int kStageElems = kStageBytes / 2;
-constexpr int kVecPerThread = kStageElems / 8 / kThreads;   // 4 x 16-byte vectors
+constexpr int kWarpVecs = kStageElems / 8 / kConsumerWarps;   // 128 vectors per warp per stage
+constexpr int kVecPerLane = kWarpVecs / 32;                   // 4
 constexpr int kStages = 4;
-constexpr int kCompactAt = 64;                       // fold the buffer beyond this many
-constexpr int kCandCap = 512 + kCompactAt;           // overflow -> the chunk is rescanned
-constexpr int kRescanVecs = 64;                      // vectors per rescan slice (512 logits)
+constexpr int kFoldAt = 32;                          // fold a warp buffer beyond this many
+constexpr int kWarpCap = kFoldAt + 32 * 8;           // + one vector (8 logits) from every lane
 
 struct TopkSmem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];   // 1-D bulk copies need 16-byte alignment
-  uint64_t cand[kCandCap];
-  uint64_t top[kTopK];        // running top-16, descending
-  uint64_t warp_top[kWarps][kTopK];
+  alignas(128) uint8_t stage[kStages][kStageBytes];  // 1-D bulk copies need 16-byte alignment
+  uint64_t cand[kConsumerWarps][kWarpCap];
+  uint64_t warp_top[kConsumerWarps][kTopK];
+  uint64_t top[kTopK];
   uint64_t full_bar[kStages];
-  uint64_t thr_key;           // top[15] (0 while fewer than 16 seen)
-  unsigned long long init_thr;  // lower bound used for a chunk that starts with no threshold
-  int count;
-  int count0;                 // count at the start of the current chunk
-  int overflow;
+  uint64_t empty_bar[kStages];
+  unsigned long long gthr;   // max over warps of their 16th-best key: a CTA-wide lower bound
+  int wcount[kConsumerWarps];
+  int abort_flag;
 };
-
-// Folds cand[0..n) into s.top using every warp; leaves s.thr_key updated and
-// s.count = 0.  Must be called by all threads of the CTA (contains __syncthreads).
-__device__ void fold_candidates(TopkSmem& s, int n, int warp, int lane) {
-  if (n <= 32) {
-    if (warp == 0) {
-      uint64_t top = lane < kTopK ? s.top[lane] : 0ull;
-      const uint64_t x = lane < n ? s.cand[lane] : 0ull;
-      top = warp_merge_top16(top, x, lane);
-      if (lane < kTopK) s.top[lane] = top;
-      if (lane == kTopK - 1) s.thr_key = top;
-      if (lane == 0) s.count = 0;
-    }
-    __syncthreads();
-    return;
-  }
-  uint64_t top = 0ull;
-  for (int base = warp * 32; base < n; base += kWarps * 32) {
-    const int i = base + lane;
-    top = warp_merge_top16(top, i < n ? s.cand[i] : 0ull, lane);
-  }
-  if (lane < kTopK) s.warp_top[warp][lane] = top;
-  __syncthreads();
-  if (warp == 0) {
-    uint64_t acc = lane < kTopK ? s.top[lane] : 0ull;
-#pragma unroll
-    for (int w = 0; w < kWarps; w += 2) {
-      const uint64_t x = (lane < kTopK) ? s.warp_top[w][lane] : s.warp_top[w + 1][lane - kTopK];
-      acc = warp_merge_top16(acc, x, lane);
-    }
-    if (lane < kTopK) s.top[lane] = acc;
-    if (lane == kTopK - 1) s.thr_key = acc;
-    if (lane == 0) s.count = 0;
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ void push_candidate(TopkSmem& s, uint64_t key) {
-  const int slot = atomicAdd(&s.count, 1);
-  if (slot < kCandCap)
-    s.cand[slot] = key;
-  else
-    s.overflow = 1;   // the chunk is rolled back and rescanned in slices
-}
-
-// Examines 8 logits (one 16-byte vector) whose first id is `id0`.
-__device__ __forceinline__ void scan_vector(TopkSmem& s, uint4 v, uint32_t id0, uint64_t thr) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t bits = h ? (w[q] >> 16) : (w[q] & 0xFFFFu);
-      const uint64_t key = make_key(bits, id0 + 2 * q + h);
-      if (key > thr) push_candidate(s, key);
-    }
-  }
-}
 
 // Max of 8 bf16 values (bf16x2 max; a NaN never wins) as bf16 bits.
 __device__ __forceinline__ uint32_t vec_max_bits(uint4 v) {
@@ -116,6 +59,47 @@ __device__ __forceinline__ uint32_t vec_max_bits(uint4 v) {
   const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
   const __nv_bfloat16 mm = __hmax(__low2bfloat16(m), __high2bfloat16(m));
   return static_cast<uint32_t>(__bfloat16_as_ushort(mm));
+}
+
+__device__ __forceinline__ uint32_t lane_elem(const uint4& v, int k) {
+  const uint32_t w = (k < 4) ? ((k < 2) ? v.x : v.y) : ((k < 6) ? v.z : v.w);
+  return (k & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// Per-warp selection state; `top` is distributed (lane i < 16 holds the i-th
+// best key, lanes 16..31 hold 0), `thr` is warp-uniform.
+struct WarpSel {
+  uint64_t top;
+  uint64_t thr;
+};
+
+// Rare path, kept out of line so the streaming loop stays small in the
+// instruction cache: every lane whose vector may qualify appends the keys
+// above `thr` to the warp's buffer.
+__device__ __noinline__ void append_vector(uint64_t* cand, int* wcount, uint4 v, uint32_t id0, uint64_t thr,
+                                           bool maybe) {
+  if (!maybe) return;
+  for (int k = 0; k < 8; ++k) {
+    const uint64_t key = make_key(lane_elem(v, k), id0 + k);
+    if (key > thr) cand[atomicAdd(wcount, 1)] = key;
+  }
+}
+
+// Folds the warp's pending candidates into its top-16 and publishes the new
+// threshold as a CTA-wide lower bound (the CTA's 16th best is at least any
+// warp's 16th best).  Whole warp.
+__device__ __noinline__ void fold_warp(WarpSel& w, uint64_t* cand, int* wcount, unsigned long long* gthr, int lane) {
+  __syncwarp();
+  const int n = *reinterpret_cast<volatile int*>(wcount);
+  for (int base = 0; base < n; base += 32)
+    w.top = warp_merge_top16(w.top, base + lane < n ? cand[base + lane] : 0ull, lane);
+  w.thr = __shfl_sync(0xFFFFFFFFu, w.top, kTopK - 1);
+  __syncwarp();
+  if (lane == 0) {
+    *wcount = 0;
+    atomicMax(gthr, static_cast<unsigned long long>(w.thr));
+  }
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __restrict__ logits,
@@ -138,122 +122,115 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
   const int n_chunks = static_cast<int>((n_vec_elems + kStageElems - 1) / kStageElems);
   const uint16_t* seg = logits + row * ld + seg_begin;
 
-  if (tid < kTopK) s.top[tid] = 0ull;
+  if (tid < kConsumerWarps) s.wcount[tid] = 0;
   if (tid == 0) {
-    s.count = 0;
-    s.count0 = 0;
-    s.overflow = 0;
-    s.thr_key = 0ull;
-    s.init_thr = 0ull;
-    for (int i = 0; i < kStages; ++i) mbar_init(&s.full_bar[i], 1);
+    s.abort_flag = 0;
+    s.gthr = 0ull;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full_bar[i], 1);
+      mbar_init(&s.empty_bar[i], kConsumerWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
+  volatile int* abort_flag = &s.abort_flag;
 
-  uint64_t policy = 0;
-  if (tid == 0) {
-    policy = l2_policy_evict_first();
-    for (int c = 0; c < kStages && c < n_chunks; ++c) {
-      const int64_t e0 = static_cast<int64_t>(c) * kStageElems;
-      const uint32_t bytes = static_cast<uint32_t>(imin64(kStageElems, n_vec_elems - e0) * 2);
-      mbar_arrive_expect_tx(&s.full_bar[c], bytes);
-      bulk_g2s(s.stage[c], seg + e0, bytes, &s.full_bar[c], policy);
-    }
-  }
-
-  int aborted_at = -1;   // CTA-uniform
-  for (int c = 0; c < n_chunks; ++c) {
-    const int st = c % kStages;
-    const uint32_t parity = static_cast<uint32_t>(c / kStages) & 1u;
-    const bool ok = mbar_wait_bounded(&s.full_bar[st], parity, err);
-    if (__syncthreads_or(!ok)) {
-      aborted_at = c;
-      break;
-    }
-    const int64_t e0 = static_cast<int64_t>(c) * kStageElems;
-    const int chunk_elems = static_cast<int>(imin64(kStageElems, n_vec_elems - e0));
-    const uint32_t id_base = static_cast<uint32_t>(seg_begin + e0);
-    const uint4* sv = reinterpret_cast<const uint4*>(s.stage[st]);
-    uint4 v[kVecPerThread];
-    uint32_t vmax[kVecPerThread];
-#pragma unroll
-    for (int h = 0; h < kVecPerThread; ++h) {
-      const int vi = tid + h * kThreads;
-      v[h] = (vi * 8 < chunk_elems) ? sv[vi] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-      vmax[h] = vec_max_bits(v[h]);
-    }
-    uint64_t thr = s.thr_key;
-    if ((thr >> 48) == 0ull) {
-      // Threshold still empty: a lower bound for this CTA's 16th best is the
-      // 16th largest of any warp's 32 per-thread maxima (16 distinct elements
-      // reach it).  Take the largest such bound over the warps.
-      // Threads without data contribute the empty key 0.
-      uint32_t tmax = 0;
-#pragma unroll
-      for (int h = 0; h < kVecPerThread; ++h)
-        if ((tid + h * kThreads) * 8 < chunk_elems) tmax = max(tmax, bf16_order(vmax[h]));
-      const uint64_t sorted = warp_sort_desc(static_cast<uint64_t>(tmax) << 48, lane);
-      if (lane == kTopK - 1) atomicMax(&s.init_thr, static_cast<unsigned long long>(sorted));
-      if (tid == 0) s.count0 = s.count;
-      __syncthreads();
-      thr = s.init_thr;
-      __syncthreads();
-      if (tid == 0) s.init_thr = 0ull;
-    } else if (tid == 0) {
-      s.count0 = s.count;
-    }
-    // elements equal to the bound keep qualifying (its id field is 0)
-    const bool exact_only = (thr >> 48) == 0ull;
-    const uint32_t thr_ord = static_cast<uint32_t>(thr >> 48);
-#pragma unroll
-    for (int h = 0; h < kVecPerThread; ++h) {
-      const int vi = tid + h * kThreads;
-      if (vi * 8 < chunk_elems && (exact_only || bf16_order(vmax[h]) >= thr_ord))
-        scan_vector(s, v[h], id_base + vi * 8, thr);
-    }
-    __syncthreads();   // stage consumed, all pushes visible
-    if (s.overflow) {
-      // Roll the chunk back (drop what it pushed), then rescan it in slices of
-      // 512 logits with a fold after each slice, so no slice can overflow.
-      const int n0 = s.count0;
-      __syncthreads();
-      fold_candidates(s, n0, warp, lane);
-      if (tid == 0) s.overflow = 0;
-      const int nvec = chunk_elems / 8;
-      for (int sl = 0; sl < nvec; sl += kRescanVecs) {
-        const uint64_t t2 = s.thr_key;
-        if (tid < kRescanVecs && sl + tid < nvec) scan_vector(s, sv[sl + tid], id_base + (sl + tid) * 8, t2);
-        __syncthreads();
-        fold_candidates(s, s.count, warp, lane);
+  if (warp == kConsumerWarps) {
+    // producer
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int issued = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int st = c % kStages;
+        if (c >= kStages && !mbar_wait_bounded(&s.empty_bar[st], ((c / kStages) - 1) & 1, err)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        const int64_t e0 = static_cast<int64_t>(c) * kStageElems;
+        const uint32_t bytes = static_cast<uint32_t>(imin64(kStageElems, n_vec_elems - e0) * 2);
+        mbar_arrive_expect_tx(&s.full_bar[st], bytes);
+        bulk_g2s(s.stage[st], seg + e0, bytes, &s.full_bar[st], policy);
+        issued = c + 1;
       }
-    }
-    if (tid == 0 && c + kStages < n_chunks) {
-      const int64_t e1 = static_cast<int64_t>(c + kStages) * kStageElems;
-      const uint32_t bytes = static_cast<uint32_t>(imin64(kStageElems, n_vec_elems - e1) * 2);
-      mbar_arrive_expect_tx(&s.full_bar[st], bytes);
-      bulk_g2s(s.stage[st], seg + e1, bytes, &s.full_bar[st], policy);
-    }
-    const int n = s.count;
-    if (n > kCompactAt) fold_candidates(s, n, warp, lane);
-  }
-
-  if (aborted_at >= 0) {
-    // Let the copies still in flight land before the CTA's shared memory goes away.
-    if (tid == 0) {
-      for (int c = aborted_at; c < n_chunks && c < aborted_at + kStages; ++c)
+      // the latest copy into every stage must land before shared memory is released
+      for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
         mbar_wait_bounded(&s.full_bar[c % kStages], static_cast<uint32_t>(c / kStages) & 1u, err);
     }
   } else {
-    // Ragged tail (segment length not a multiple of 8): plain loads.
-    const int64_t tail = n_elems - n_vec_elems;
-    if (tid < tail) {
-      const int64_t e = n_vec_elems + tid;
-      const uint64_t key = make_key(seg[e], static_cast<uint32_t>(seg_begin + e));
-      if (key > s.thr_key) push_candidate(s, key);
+    // consumer warp
+    WarpSel w{0ull, 0ull};
+    uint64_t* cand = s.cand[warp];
+    int* wcount = &s.wcount[warp];
+    for (int c = 0; c < n_chunks; ++c) {
+      const int st = c % kStages;
+      if (!mbar_wait_bounded(&s.full_bar[st], static_cast<uint32_t>(c / kStages) & 1u, err) || *abort_flag) {
+        *abort_flag = 1;
+        break;
+      }
+      const int64_t e0 = static_cast<int64_t>(c) * kStageElems;
+      const int chunk_vecs = static_cast<int>(imin64(kStageElems, n_vec_elems - e0)) / 8;
+      const uint4* sv = reinterpret_cast<const uint4*>(s.stage[st]);
+      uint4 v[kVecPerLane];
+      uint32_t vord[kVecPerLane];
+      bool real[kVecPerLane];
+#pragma unroll
+      for (int h = 0; h < kVecPerLane; ++h) {
+        const int vi = warp * kWarpVecs + h * 32 + lane;
+        real[h] = vi < chunk_vecs;
+        v[h] = real[h] ? sv[vi] : make_uint4(0u, 0u, 0u, 0u);
+        vord[h] = real[h] ? bf16_order(vec_max_bits(v[h])) : 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty_bar[st]);   // the stage may be refilled now
+      const uint64_t g = *reinterpret_cast<volatile unsigned long long*>(&s.gthr);
+      if (g > w.thr) w.thr = g;
+      if ((w.thr >> 48) == 0ull) {
+        // No threshold yet: the 16th largest of the 32 lane maxima is a lower
+        // bound for this warp's 16th best (16 distinct elements reach it);
+        // lanes without data contribute the empty key 0.
+        uint32_t lm = 0u;
+#pragma unroll
+        for (int h = 0; h < kVecPerLane; ++h) lm = max(lm, vord[h]);
+        const uint64_t sorted = warp_sort_desc(static_cast<uint64_t>(lm) << 48, lane);
+        w.thr = __shfl_sync(0xFFFFFFFFu, sorted, kTopK - 1);
+      }
+#pragma unroll
+      for (int h = 0; h < kVecPerLane; ++h) {
+        const uint32_t thr_ord = static_cast<uint32_t>(w.thr >> 48);
+        const bool maybe = real[h] && (thr_ord == 0u || vord[h] >= thr_ord);
+        if (__ballot_sync(0xFFFFFFFFu, maybe) == 0u) continue;
+        const uint32_t id0 = static_cast<uint32_t>(seg_begin + e0) + (warp * kWarpVecs + h * 32 + lane) * 8;
+        append_vector(cand, wcount, v[h], id0, w.thr, maybe);
+        __syncwarp();
+        if (*reinterpret_cast<volatile int*>(wcount) > kFoldAt) fold_warp(w, cand, wcount, &s.gthr, lane);
+      }
+      // Fold whatever the chunk left at its end: the threshold then tracks the
+      // 16th best seen so far and the CTA-wide bound rises with it.
+      __syncwarp();
+      if (*reinterpret_cast<volatile int*>(wcount) > 0) fold_warp(w, cand, wcount, &s.gthr, lane);
     }
-    __syncthreads();
-    const int n = s.count;
-    if (n > 0) fold_candidates(s, n, warp, lane);
+    if (warp == 0 && !*abort_flag) {
+      // ragged tail (segment length not a multiple of 8): plain loads
+      const int64_t tail = n_elems - n_vec_elems;
+      if (lane < tail) {
+        const int64_t e = n_vec_elems + lane;
+        const uint64_t key = make_key(seg[e], static_cast<uint32_t>(seg_begin + e));
+        if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
+      }
+    }
+    fold_warp(w, cand, wcount, &s.gthr, lane);
+    if (lane < kTopK) s.warp_top[warp][lane] = w.top;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t acc = 0ull;
+#pragma unroll
+    for (int ww = 0; ww < kConsumerWarps; ww += 2) {
+      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
+      acc = warp_merge_top16(acc, x, lane);
+    }
+    if (lane < kTopK) s.top[lane] = acc;
   }
 
   // Merge the cluster's partial lists in distributed shared memory.
@@ -281,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(const uint16_t* __rest
 
 int topk_cluster_size(int64_t rows, int64_t V, int num_sms) {
   // Enough CTAs for ~3 resident per SM, never a segment under one stage.
-  const int64_t want = (3LL * num_sms + rows - 1) / rows;
+  const int64_t want = (3LL * num_sms + rows - 1) / rows;   // ~3 resident CTAs per SM
   int S = 1;
   while (S < want && S < 16) S <<= 1;
   while (S > 1 && (V + S - 1) / S < kStageElems) S >>= 1;

@@ -132,8 +132,10 @@ __device__ int32_t row_argmax(VerifySmem& s, const uint16_t* row, int64_t V, con
     for (int u = 0; u < 4; ++u) v[u] = ldg_stream(rv + i + u * kVThreads);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
+      // a vector only matters if its max beats the thread's best so far (a tie
+      // with it has a larger id, and ids increase along the thread's stripe)
       const uint32_t vo = bf16_order(vec_max_bits(v[u]));
-      if (vo >= static_cast<uint32_t>(best >> 32)) {
+      if (vo > static_cast<uint32_t>(best >> 32)) {
         const uint32_t id0 = static_cast<uint32_t>((i + u * kVThreads) * 8);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -156,7 +158,8 @@ __device__ int32_t row_argmax(VerifySmem& s, const uint16_t* row, int64_t V, con
     best = kmax(best, (static_cast<uint64_t>(bf16_order(row[e])) << 32) |
                           static_cast<uint64_t>(~static_cast<uint32_t>(e)));
   const uint64_t r = block_max_key(s, best);
-  return static_cast<int32_t>(~static_cast<uint32_t>(r));
+  // an all-NaN row never sets a key: its arg-max is the lowest id, 0
+  return r == 0ull ? 0 : static_cast<int32_t>(~static_cast<uint32_t>(r));
 }
 
 // Softmax statistics of one row at inverse-temperature c = log2(e) / T:

@@ -187,15 +187,19 @@ int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const 
 
 /*
  * Fused LM head + top-16: logits = hidden W^T are produced tile by tile on the
- * tensor cores and reduced to each row's top-16 on chip, so no logit reaches
- * global memory (the head produces U_t, "DFlash's own logit").
+ * tensor cores (tcgen05, fp32 accumulation) and reduced to each row's top-16
+ * on chip, so no logit reaches global memory (the head produces U_t, "DFlash's
+ * own logit").
  *   hidden  device bf16 [M, d];  W device bf16 [V, d]
- *   vals    device fp32 [M, 16];  idx device int32 [M, 16] (order as dflash2_topk)
- *   workspace  device, >= dflash2_lmhead_topk_workspace(M, V, d) bytes, 256-byte
- *              aligned; holds per-tile partial lists, fully rewritten per call.
- * d % 64 == 0, M >= 1, V >= 16.
+ *   vals    device fp32 [M, 16] (the fp32 logits);  idx device int32 [M, 16]
+ *           (value descending, lowest id on ties)
+ *   workspace  device scratch of at least dflash2_lmhead_topk_workspace(h, M, V, d)
+ *              bytes, 256-byte aligned: per-CTA partial lists, fully rewritten
+ *              by every call; calls that overlap on the GPU must not share it.
+ * d % 64 == 0, V >= 16.  The workspace size depends on the device's SM count,
+ * hence the handle argument (0 for a null handle or empty problem).
  */
-size_t dflash2_lmhead_topk_workspace(int64_t M, int64_t V, int64_t d);
+size_t dflash2_lmhead_topk_workspace(const dflash2_handle* h, int64_t M, int64_t V, int64_t d);
 int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
                         int64_t V, int64_t d, float* vals, int32_t* idx, void* workspace,
                         size_t ws_bytes, void* stream);
