@@ -29,7 +29,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from draft_selection_dflash2_gb300 import synth  # noqa: E402
+from draft_selection_dflash2_gb300 import replicas, synth  # noqa: E402
 
 METRIC = "draft blocks/s"
 UNIT = "blocks/s"
@@ -136,20 +136,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def make_host_workload(nb, sweep_rows=0):
-    """Seeded host tensors of the full-cycle workload (bf16 as uint16 bits)."""
-    rng = np.random.default_rng(0)
+def make_host_workload(nb, sweep_rows=0, rank=0):
+    """Seeded host tensors of the full-cycle workload (bf16 as uint16 bits).
+    Per-sequence data depends on the rank (each replica drafts its own batch);
+    the parameters (conv kernels, W_H, A, B) are shared."""
+    sd = lambda s: replicas.rank_seed(s, rank)  # noqa: E731
+    rng = np.random.default_rng(sd(0))
     rows = max(nb * L, sweep_rows)
     w = {}
     w["U"] = synth.logits_planted(rng, rows, V)
     # each conv application reads its own activation (in the drafter every
     # sublayer boundary presents a new hidden state), so nothing is chained
-    w["conv"] = [(synth.normal_bits(100 + a, (nb, L, D)), synth.normal_bits(200 + a, (nb, D)))
+    w["conv"] = [(synth.normal_bits(sd(100 + a), (nb, L, D)), synth.normal_bits(sd(200 + a), (nb, D)))
                  + synth.conv_layer_params(10 + a, D) for a in range(CONV_APPS)]
     w["W_H"] = synth.normal_bits(3, (R, D), std=0.02)
     w["A"] = synth.normal_bits(4, (V, R), std=0.02)
     w["Bt"] = synth.normal_bits(5, (V, R), std=0.02)
-    w["last_verified"] = np.random.default_rng(6).integers(0, V, nb).astype(np.int32)
+    w["last_verified"] = np.random.default_rng(sd(6)).integers(0, V, nb).astype(np.int32)
     return w
 
 
@@ -231,14 +234,14 @@ def run_gpu(args):
     h = api.Handle(torch.cuda.current_device())
 
     sweep_rows = max(SWEEP_B) * L if (args.sweep and rank == 0) else 0
-    w = make_host_workload(B, sweep_rows)
+    w = make_host_workload(B, sweep_rows, rank)
     cyc = Cycle(torch, api, h, w, B, dev)
     # plant the target on the greedy draft of one untimed cycle: 0.85 argmax agreement
     cyc.target = torch.empty((B, L + 1, V), dtype=torch.bfloat16, device=dev)
     cyc.step()
     torch.cuda.synchronize()
     draft = cyc.tok[0].cpu().numpy()
-    tgt = synth.target_planted(7, draft, V, agree=0.85, plant=8.0)
+    tgt = synth.target_planted(replicas.rank_seed(7, rank), draft, V, agree=0.85, plant=8.0)
     cyc.target.copy_(to_dev(torch, tgt, dev))
     stream = torch.cuda.current_stream()
 
@@ -264,11 +267,7 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = replicas.max_over_ranks(t0.elapsed_time(t1), dist, dev)
     assert h.device_error() == 0, "device error during the timed region"
 
     stage_ms = {}
@@ -279,7 +278,7 @@ def run_gpu(args):
     acc0 = cyc.acc[0].cpu().numpy()
     acc1 = cyc.acc[1].cpu().numpy()
 
-    value = world * B * args.steps / (elapsed_ms / 1e3)
+    value = replicas.whole_job_rate(B * args.steps, world, elapsed_ms / 1e3)
     ms_per_step = elapsed_ms / args.steps
     hbm = pk["hbm_gbs"]
     stage_bytes = {"conv": CONV_APPS * bytes_conv(B), "topk": bytes_topk(B), "pairs": bytes_pairs(B),
