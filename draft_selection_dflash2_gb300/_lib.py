@@ -34,6 +34,7 @@ SIGNATURES = {
     "dflash2_verify": (I32, [P, P, I64, P, P, P, P, I64, I64, I64, F32, U64, U64, P, P, P]),
     "dflash2_lmhead_topk_workspace": (SZ, [P, I64, I64, I64]),
     "dflash2_lmhead_topk": (I32, [P, P, P, I64, I64, I64, P, P, P, SZ, P]),
+    "dflash2_lmhead_topk_noalloc": (I32, [P, P, P, I64, I64, I64, P, P, P]),
 }
 
 _lib = None

@@ -194,3 +194,18 @@ def lmhead_topk(h: Handle, hidden, W, vals=None, idx=None, workspace=None, strea
                                       _ptr(workspace), workspace.numel(), _stream(stream)),
            "dflash2_lmhead_topk")
     return vals, idx
+
+
+def lmhead_topk_noalloc(h: Handle, hidden, W, vals=None, idx=None, stream=None):
+    """lmhead_topk for callers that cannot allocate: the library's fixed
+    device scratch replaces the workspace (calls sharing a device must not
+    overlap on the GPU).  Outputs not passed in are allocated here, by torch."""
+    M, d = hidden.shape
+    V = W.shape[0]
+    dev = hidden.device
+    vals = torch.empty((M, K), dtype=torch.float32, device=dev) if vals is None else vals
+    idx = torch.empty((M, K), dtype=torch.int32, device=dev) if idx is None else idx
+    _check(h._lib.dflash2_lmhead_topk_noalloc(h.ptr, _ptr(hidden), _ptr(W), M, V, d, _ptr(vals), _ptr(idx),
+                                              _stream(stream)), "dflash2_lmhead_topk_noalloc")
+    return vals, idx
+

@@ -208,4 +208,20 @@ int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_
                                               h->err, as_stream(stream)));
 }
 
+int dflash2_lmhead_topk_noalloc(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
+                                int64_t V, int64_t d, float* vals, int32_t* idx, void* stream) {
+  if (bad_handle(h) || M < 0 || V < 0 || d <= 0) return DFLASH2_ERR_INVALID_ARG;
+  if (d % 64 != 0 || V < kK || V >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
+  if (M == 0) return DFLASH2_OK;
+  if (!hidden || !W || !vals || !idx) return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(vals, 4) || !aligned(idx, 4))
+    return DFLASH2_ERR_MISALIGNED;
+  if (dflash2::lmhead_workspace_bytes(M, V, d, h->num_sms) > dflash2::kLmheadNoAllocScratchBytes)
+    return DFLASH2_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (dflash2::lmhead_noalloc_scratch(h->device, &scratch) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  return launched(dflash2::launch_lmhead_topk(hidden, W, M, V, d, vals, idx, scratch, h->num_sms, h->err,
+                                              as_stream(stream)));
+}
+
 }  // extern "C"

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dflash2.h"
+
 namespace dflash2 {
 
 int topk_cluster_size(int64_t rows, int64_t V, int num_sms);
@@ -33,6 +35,8 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
                           int num_sms, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms);
+constexpr size_t kLmheadNoAllocScratchBytes = DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES;
+cudaError_t lmhead_noalloc_scratch(int device, void** ptr);
 cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,
                                int64_t d, float* vals, int32_t* idx, void* workspace,
                                int num_sms, uint32_t* err, cudaStream_t stream);

@@ -23,6 +23,8 @@
 //   (fp32 value, -id) to the workspace [M, n_runs, 16].
 // lmhead_merge_kernel: one warp per row folds the n_runs partial lists into the
 // final top-16 (value descending, lowest id on ties).
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tcgen05.cuh"
@@ -273,6 +275,37 @@ LmPlan lm_plan(int64_t M, int64_t V, int num_sms) {
 }
 
 }  // namespace
+
+// Fixed scratch for dflash2_lmhead_topk_noalloc: the partial lists live in
+// this file-scope device array instead of a caller-provided workspace.  Every
+// GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_lmhead_scratch[kLmheadNoAllocScratchBytes];
+
+cudaError_t lmhead_noalloc_scratch(int device, void** ptr) {
+  // The array's device address, looked up once per device with that device
+  // current (its host-side name is only a stand-in for the symbol).
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[device] == nullptr) {
+    int prev = -1;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return e;
+    if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_lmhead_scratch);
+    if (prev != device) {
+      const cudaError_t e2 = cudaSetDevice(prev);
+      if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return e;
+    addr[device] = p;
+  }
+  *ptr = addr[device];
+  return cudaSuccess;
+}
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms) {
   (void)d;

@@ -204,6 +204,33 @@ int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_
                         int64_t V, int64_t d, float* vals, int32_t* idx, void* workspace,
                         size_t ws_bytes, void* stream);
 
+/*
+ * dflash2_lmhead_topk without a workspace argument, for callers that cannot
+ * allocate device memory: code running inside an engine whose memory pool owns
+ * every byte of the GPU, or a latency-critical serving loop where a cudaMalloc
+ * or cudaFree (which may synchronise the device) is not acceptable.  The pages
+ * have no counterpart of this call; it exists for those callers only.
+ *
+ * The partial lists go to a fixed scratch array of
+ * DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES bytes that the library declares as a
+ * file-scope device variable: every GPU that loads the library holds it until
+ * the process exits.  A problem whose partial lists exceed it (more than
+ * DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES / 128 row-runs; 1024 hidden rows fit on
+ * any GPU with at most 256 SMs) is rejected with DFLASH2_ERR_WORKSPACE before
+ * anything runs.  The call allocates nothing.
+ *
+ * The first call on a device looks up the scratch array's device address (with
+ * that device made current for the lookup, then restored); make that first
+ * call before any stream capture.  All calls share the one array and every
+ * call rewrites the part it uses, so nothing needs clearing, but calls that
+ * overlap on the GPU (different streams, or different handles of the same
+ * device) race on it and must be serialised by the caller.  Arguments, output
+ * layout and errors are otherwise those of dflash2_lmhead_topk.
+ */
+#define DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dflash2_lmhead_topk_noalloc(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
+                                int64_t V, int64_t d, float* vals, int32_t* idx, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
