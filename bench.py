@@ -77,6 +77,62 @@ def bytes_walk(nb):
 
 
 # ---------------------------------------------------------------------------
+# DRAM traffic per launch from the committed ncu summaries, valid only while
+# the kernel's sources are unchanged since the capture (else null)
+# ---------------------------------------------------------------------------
+_CSRC = os.path.join(ROOT, "draft_selection_dflash2_gb300", "csrc")
+_PROFILED = {
+    "conv": ["conv2tap_B128_d5120.md"],
+    "topk": ["topk16_B128_V151936.md"],
+    "pairs": ["gate_gemm_B128_d5120.md", "pair_kernel_B128.md"],
+    "verify0": ["verify_rows_T0_B128.md"],
+    "verify1": ["verify_rows_T1_B128.md"],
+    "walk1": ["walk_T1_B128.md"],
+}
+_SOURCES = {
+    "topk16": ["topk.cu", "common.cuh"],
+    "conv2tap": ["conv2tap.cu", "gemm_tc.cuh", "tcgen05.cuh", "common.cuh"],
+    "verify_rows": ["verify.cu", "common.cuh", "philox.cuh"],
+    "pair_scores": ["select.cu", "gemm_tc.cuh", "tcgen05.cuh", "common.cuh"],
+    "walk": ["walk.cu", "common.cuh", "philox.cuh"],
+    "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
+}
+_PROFILE_SOURCES = {"conv2tap_B128_d5120.md": "conv2tap", "topk16_B128_V151936.md": "topk16",
+                    "gate_gemm_B128_d5120.md": "pair_scores", "pair_kernel_B128.md": "pair_scores",
+                    "verify_rows_T0_B128.md": "verify_rows", "verify_rows_T1_B128.md": "verify_rows",
+                    "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead"}
+
+
+def _source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in _SOURCES[kernel]:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(names):
+    """Sum of dram bytes per launch over the named summaries, or None if any is
+    missing or was captured from different kernel sources."""
+    total = 0
+    for name in names:
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            return None
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.split(":")[0] in ("dram-bytes-per-launch", "source-sha256"):
+                    k, v = line.split(":", 1)
+                    fields[k] = v.strip()
+        if fields.get("source-sha256") != _source_hash(_PROFILE_SOURCES[name]):
+            return None
+        total += int(fields["dram-bytes-per-launch"])
+    return total
+
+
+# ---------------------------------------------------------------------------
 # clocks sampled with nvidia-smi during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
@@ -297,8 +353,11 @@ def run_gpu(args):
     per_launch_ms = stage_ms[dom] / (CONV_APPS if dom == "conv" else 1)
     per_launch_bytes = stage_bytes[dom] / (CONV_APPS if dom == "conv" else 1)
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(_PROFILED[dom]) if dom in _PROFILED else None
     roofline = {"bound": "hbm", "kernel": kernel_name, "stage": dom, "achieved": round(achieved, 1),
-                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": traffic, "traffic_unit": "bytes per launch (ncu, profiles/)",
+                "alg_bytes_per_launch": int(per_launch_bytes),
                 "peak_source": pk["source"] + " (burst copy, MEASURED_PEAKS.json)"}
 
     line = {
@@ -412,6 +471,7 @@ def run_lmhead(torch, api, h, dev, pk, M=1024):
     tf = flops / (fused_ms * 1e-3) / 1e12
     del logits, W, hidden
     return {"workload": f"fused LM-head top-16 M={M} d={D} V={V}", "fused_ms": round(fused_ms, 4),
+            "traffic": profiled_traffic(["lmhead_M1024_V151936_d5120.md"]),
             "unfused_cublas_plus_topk_ms": round(unfused_ms, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
