@@ -91,9 +91,9 @@ _PROFILED = {
 }
 _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
-    "conv2tap": ["conv2tap.cu", "gemm_tc.cuh", "tcgen05.cuh", "common.cuh"],
+    "conv2tap": ["conv2tap.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "verify_rows": ["verify.cu", "common.cuh", "philox.cuh"],
-    "pair_scores": ["select.cu", "gemm_tc.cuh", "tcgen05.cuh", "common.cuh"],
+    "pair_scores": ["select.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "walk": ["walk.cu", "common.cuh", "philox.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
 }
@@ -347,7 +347,8 @@ def run_gpu(args):
                      "frac_hbm": round(gbs / hbm, 4)}
     stages["conv"]["per_application_ms"] = round(stage_ms["conv"] / CONV_APPS, 4)
     dom = max(STAGES, key=lambda n: stage_ms[n])
-    kernel_name = {"conv": "conv2tap_kernel", "topk": "topk16_kernel", "pairs": "gate_kernel + pair_kernel",
+    kernel_name = {"conv": "splitk_gemm_kernel<ConvEpi>", "topk": "topk16_kernel",
+                   "pairs": "splitk_gemm_kernel<GateEpi> + pair_kernel",
                    "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_rows_kernel",
                    "verify1": "verify_rows_kernel"}[dom]
     per_launch_ms = stage_ms[dom] / (CONV_APPS if dom == "conv" else 1)

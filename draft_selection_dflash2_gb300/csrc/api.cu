@@ -131,7 +131,7 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
       !aligned(last_verified, 4) || (b_H && !aligned(b_H, 4)))
     return DFLASH2_ERR_MISALIGNED;
   cudaStream_t s = as_stream(stream);
-  int st = launched(dflash2::launch_gate(hs, W_H, b_H, B * L, d, gate, h->err, s));
+  int st = launched(dflash2::launch_gate(hs, W_H, b_H, B * L, d, gate, h->err, h->num_sms, s));
   if (st != DFLASH2_OK) return st;
   return launched(dflash2::launch_pair_scores(cand_idx, cand_val, last_verified, gate, A, Bt, B, L, V,
                                               S, h->err, s));
@@ -164,7 +164,7 @@ int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_pre
       !aligned(k1, 16) || !aligned(W_c, 16) || !aligned(y, 16) || (b_c && !aligned(b_c, 4)))
     return DFLASH2_ERR_MISALIGNED;
   return launched(dflash2::launch_conv2tap(x, x_prev, hs, k0, k1, W_c, b_c, B, L, d, y, y_is_fp32,
-                                           h->err, as_stream(stream)));
+                                           h->err, h->num_sms, as_stream(stream)));
 }
 
 int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const int32_t* draft_tok,

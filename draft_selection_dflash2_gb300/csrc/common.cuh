@@ -45,6 +45,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Rounds a dynamic shared-memory base up to kAlign bytes by pointer arithmetic
+// on the shared array itself: the compiler then still knows that the result,
+// and every pointer derived from it, addresses shared memory, and emits
+// shared-memory instructions for the accesses (a round trip through an
+// integer would turn each of them into a slower generic access).
+template <int kAlign>
+__device__ __forceinline__ uint8_t* align_smem(uint8_t* base) {
+  return base + ((kAlign - (smem_addr(base) & (kAlign - 1))) & (kAlign - 1));
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }

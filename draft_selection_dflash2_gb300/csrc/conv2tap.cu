@@ -7,20 +7,29 @@
 //   [c0; c1][m, :] = W_c h[m, :] (+ b_c)            W_c: [2G, d], G = d / 16
 //   y[m, ch] = (k0[ch] + c0[m, ch/16]) x[m, ch] + (k1[ch] + c1[m, ch/16]) xp[ch]
 //
-// One fused kernel: the correction is a [M, d] x [d, 2G] contraction on the
-// tensor cores (tcgen05 GEMM, fp32 accumulator in TMEM).  A CTA owns 128
-// positions x 32 groups: its B tile is W_c rows [g0, g0+32) (-> c0) stacked on
-// rows [G+g0, G+g0+32) (-> c1), so both coefficients of its 512 channels meet in
-// one accumulator.  The epilogue parks the 64 correction columns in shared
-// memory and then sweeps the 128 x 512 channel tile with coalesced 16-byte
-// loads of x_t / x_{t-1} and 16-byte stores of y; the correction never leaves
-// the SM.
+// One fused kernel (gemm_splitk.cuh): the correction is a [M, d] x [d, 2G]
+// contraction on the tensor cores, tiled as 128 positions x BNG groups; the
+// tile's B operand stacks W_c rows [g0, g0+BNG) (-> c0) on rows [G+g0, G+g0+BNG)
+// (-> c1), so both coefficients of the tile's 16*BNG channels meet in one
+// accumulator.  The K loop is split over a cluster of ks CTAs whose fp32
+// partials meet through distributed shared memory.  Cluster rank r then owns
+// 128/ks rows: it sums their slots once, and stages the rows' x_t in shared
+// memory with bulk copies (all of them in one pass when they fit, as they do
+// for d = 5120), together with the previous-tap rows that are not the row
+// above (the pass's first row, and every first position, whose previous tap
+// is x_prev[b]).  Every (row, 8 channels) item is then independent: its two
+// taps come from shared memory (or, for consecutive rows of one thread, the
+// register that held the row above), and y leaves with 16-byte stores.  The
+// correction never leaves the SMs.
 #include "common.cuh"
-#include "gemm_tc.cuh"
+#include "gemm_splitk.cuh"
 #include "launch.h"
 
 namespace dflash2 {
 namespace {
+
+constexpr int kMaxGroupsPerTile = 160;   // BN = 2 * BNG <= 320 (two N = 160 MMAs)
+constexpr int kPrevTableBytes = 512;     // previous-tap row offsets of one pass (<= 128 rows), end of the region
 
 struct ConvEpi {
   struct Params {
@@ -31,102 +40,177 @@ struct ConvEpi {
     const float* b_c;         // [2G] or null
     void* y;                  // [M, d] bf16 or fp32
     int y_is_fp32;
-    int M, L, d, G;
+    int M, L, d, G, BNG;
+    int PR;                   // x_t rows per pass; the staged previous-tap rows follow them
+    int stage_off;            // byte offset of the pass buffer in the region
   };
-  static constexpr int kGroups = 32;            // groups per CTA (512 channels)
-  static constexpr int kBN = 2 * kGroups;       // c0 | c1 columns
-  static constexpr int kPitch = kBN + 1;        // fp32 words per row in shared memory
-  static constexpr int kSmemBytes = 128 * kPitch * 4;
 
-  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, const Params& p, uint64_t* bar,
+  __host__ __device__ static int sub_n(int BN) { return BN > 256 ? BN / 2 : BN; }
+
+  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, int n_tile, const Params& p, uint64_t* bar,
                                 uint64_t pol) {
-    const int g0 = blockIdx.y * kGroups;
-    tma_load_2d(dst, tm, k, g0, bar, pol);                                             // c0 rows
-    tma_load_2d(static_cast<uint8_t*>(dst) + kGroups * kTileRowBytes, tm, k, p.G + g0, bar, pol);  // c1 rows
+    const int g0 = n_tile * p.BNG;
+    tma_load_2d(dst, tm, k, g0, bar, pol);                                                // c0 rows
+    tma_load_2d(static_cast<uint8_t*>(dst) + p.BNG * kTileRowBytes, tm, k, p.G + g0, bar, pol);  // c1 rows
   }
 
-  __device__ static void consume(const Params& p, uint8_t* smem, int, int row_local, int c, const float (&v)[32]) {
-    float* csm = reinterpret_cast<float*>(smem) + row_local * kPitch + c * kGroups;
-    const int g0 = blockIdx.y * kGroups;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int g = g0 + i;
-      float bias = 0.0f;
-      if (p.b_c && g < p.G) bias = p.b_c[c * p.G + g];
-      csm[i] = v[i] + bias;
+  // Staged previous-tap rows of a pass of n rows starting at row mb: the
+  // pass's row 0, then every row j >= 1 at a first position ((mb + j) % L == 0),
+  // in row order; prev_index(j) is such a row's place among them.
+  __device__ static int staged_prev_count(int mb, int n, int L) { return 1 + (mb + n - 1) / L - mb / L; }
+  __device__ static int prev_index(int mb, int j, int L) { return j == 0 ? 0 : 1 + (mb + j - 1) / L - mb / L; }
+
+  __device__ static __forceinline__ void issue_pass(const Params& p, uint8_t* buf, uint64_t* bar, int mb, int n,
+                                                    int g0, uint32_t cpy, uint64_t pol) {
+    const int rowb = p.BNG * 32;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n + staged_prev_count(mb, n, p.L)) * cpy);
+    const uint16_t* xs = p.x + static_cast<int64_t>(mb) * p.d + g0 * 16;   // row mb + j at xs + j * d
+    int t = mb % p.L, b = mb / p.L, k = 1;                                    // position, sequence, next prev slot
+    for (int j = 0; j < n; ++j) {
+      bulk_g2s(buf + j * rowb, xs + static_cast<int64_t>(j) * p.d, cpy, bar, pol);
+      if (t == 0 || j == 0) {
+        const uint16_t* src = t == 0 ? p.x_prev + static_cast<int64_t>(b) * p.d + g0 * 16
+                                     : xs + static_cast<int64_t>(j - 1) * p.d;
+        bulk_g2s(buf + (p.PR + (j == 0 ? 0 : k++)) * rowb, src, cpy, bar, pol);
+      }
+      if (++t == p.L) {
+        t = 0;
+        ++b;
+      }
     }
   }
 
-  // All 192 threads sweep the 128 x (16 * ng) channel tile in 8-channel vectors;
-  // each thread issues the loads of kUnroll vectors before using any of them.
-  static constexpr int kUnroll = 4;
+  // 8 bf16 values (one 16-byte vector) as floats
+  __device__ static __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = __uint_as_float(w[q] << 16);
+      f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
 
-  __device__ static void finish(const Params& p, uint8_t* smem, int m0, int tid) {
-    const float* csm = reinterpret_cast<const float*>(smem);
-    const int g0 = blockIdx.y * kGroups;
-    const int ng = (p.G - g0 < kGroups) ? p.G - g0 : kGroups;
-    const int vec_per_row = 2 * ng;                 // 8-channel vectors per row
-    const int rows = (p.M - m0 < 128) ? p.M - m0 : 128;
-    const int total = rows * vec_per_row;
-    for (int e0 = tid; e0 < total; e0 += kUnroll * kGemmThreads) {
-      uint4 xv[kUnroll], pv[kUnroll], a0v[kUnroll], a1v[kUnroll];
+  // y[m, ch .. ch+8) from 8 channels of x_t, x_{t-1}, the unpacked k0, k1 and the
+  // group's coefficients: (k0 + c0) x_t + (k1 + c1) x_{t-1}, in fp32.
+  __device__ static __forceinline__ void write8(const Params& p, int64_t m, int64_t ch, uint4 xv, uint4 pv,
+                                                const float (&k0f)[8], const float (&k1f)[8], float c0, float c1) {
+    float xt[8], xp[8], out[8];
+    unpack8(xv, xt);
+    unpack8(pv, xp);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int e = e0 + u * kGemmThreads;
-        if (e >= total) continue;
-        const int r = e / vec_per_row, cv = e % vec_per_row;
-        const int m = m0 + r;
-        const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
-        const int t = m % p.L;
-        const uint16_t* prow = t > 0 ? p.x + static_cast<int64_t>(m - 1) * p.d : p.x_prev + (m / p.L) * static_cast<int64_t>(p.d);
-        xv[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(m) * p.d + ch);
-        pv[u] = *reinterpret_cast<const uint4*>(prow + ch);
-        a0v[u] = __ldg(reinterpret_cast<const uint4*>(p.k0 + ch));
-        a1v[u] = __ldg(reinterpret_cast<const uint4*>(p.k1 + ch));
+    for (int i = 0; i < 8; ++i) out[i] = fmaf(k0f[i] + c0, xt[i], (k1f[i] + c1) * xp[i]);
+    const int64_t o = m * p.d + ch;
+    if (p.y_is_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+      dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+      dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(out[2 * q], out[2 * q + 1]);
+        w[q] = *reinterpret_cast<const uint32_t*>(&h2);
       }
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+
+  __device__ static __forceinline__ void finish(const Params& p, const SplitKShape& sh, uint8_t* region,
+                                                uint64_t* bars, int m0, int n_tile, int rank, int tid, uint32_t* err) {
+    const int rows_per = 128 / sh.ks;
+    const int pitch = sk_partial_pitch(sh.BN);
+    float* sums = reinterpret_cast<float*>(region);
+    const int g0 = n_tile * p.BNG;
+    const int ng = (p.G - g0 < p.BNG) ? p.G - g0 : p.BNG;
+    const int mb = m0 + rank * rows_per;                       // this rank's first row
+    const int nrows = p.M - mb >= rows_per ? rows_per : (p.M - mb > 0 ? p.M - mb : 0);
+
+    // 1. slot 0 <- the sum of the slots (each element is read and written by one thread)
+    if (sh.ks > 1) {
+      const SkPartials parts(sums, sh.ks, pitch);
+      const int c4n = sh.BN / 4;
+      const int total = nrows * c4n;
+      for (int e0 = tid; e0 < total; e0 += 2 * kSkThreads) {
+        float4 v[2];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int e = e0 + u * kGemmThreads;
-        if (e >= total) continue;
-        const int r = e / vec_per_row, cv = e % vec_per_row;
-        const int m = m0 + r;
-        const int gl = cv >> 1;
-        const int64_t ch = static_cast<int64_t>(g0) * 16 + cv * 8;
-        const float c0 = csm[r * kPitch + gl];
-        const float c1 = csm[r * kPitch + kGroups + gl];
-        const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-        const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
-        const uint32_t k0w[4] = {a0v[u].x, a0v[u].y, a0v[u].z, a0v[u].w};
-        const uint32_t k1w[4] = {a1v[u].x, a1v[u].y, a1v[u].z, a1v[u].w};
-        float out[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int sh = h * 16;
-            const float xt = bf16_bits_to_float((xw[q] >> sh) & 0xFFFFu);
-            const float xp = bf16_bits_to_float((pw[q] >> sh) & 0xFFFFu);
-            const float a0 = bf16_bits_to_float((k0w[q] >> sh) & 0xFFFFu) + c0;
-            const float a1 = bf16_bits_to_float((k1w[q] >> sh) & 0xFFFFu) + c1;
-            out[2 * q + h] = fmaf(a0, xt, a1 * xp);
-          }
+        for (int u = 0; u < 2; ++u) {
+          const int e = e0 + u * kSkThreads;
+          if (e < total) v[u] = parts.sum4(e / c4n, (e % c4n) * 4);
         }
-        const int64_t o = static_cast<int64_t>(m) * p.d + ch;
-        if (p.y_is_fp32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
-          dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-          dst[1] = make_float4(out[4], out[5], out[6], out[7]);
-        } else {
-          uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q]));
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(out[2 * q + 1]));
-            w[q] = lo | (hi << 16);
-          }
-          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 2; ++u) {
+          const int e = e0 + u * kSkThreads;
+          if (e < total) *reinterpret_cast<float4*>(sums + (e / c4n) * pitch + (e % c4n) * 4) = v[u];
         }
       }
+    }
+    __syncthreads();   // the other slots are free from here on
+
+    // 2. passes of up to PR rows through one buffer.  Thread -> 8-channel unit
+    //    u = tid % 2ng (its k0, k1 and bias stay in registers) and rows
+    //    j = tid / 2ng + i * R, R = threads / 2ng; with R == 1 (d = 5120) a thread
+    //    walks consecutive rows and carries x_t over as the next row's x_{t-1}.
+    uint8_t* buf = region + p.stage_off;
+    int* prev_off = reinterpret_cast<int*>(region + sh.region_bytes - kPrevTableBytes);   // per row of a pass
+    const int rowb = p.BNG * 32;
+    const uint32_t cpy = static_cast<uint32_t>(ng) * 32;
+    const int nu = 2 * ng;
+    const int R = kSkThreads / nu;
+    const bool active = tid < R * nu;
+    const int u = tid % nu, r0 = tid / nu;
+    uint4 k0v = make_uint4(0, 0, 0, 0), k1v = k0v;
+    float b0 = 0.0f, b1 = 0.0f;
+    float k0f[8], k1f[8];
+    if (active) {
+      k0v = __ldg(reinterpret_cast<const uint4*>(p.k0 + static_cast<int64_t>(g0) * 16) + u);
+      k1v = __ldg(reinterpret_cast<const uint4*>(p.k1 + static_cast<int64_t>(g0) * 16) + u);
+      if (p.b_c) {
+        b0 = p.b_c[g0 + (u >> 1)];
+        b1 = p.b_c[p.G + g0 + (u >> 1)];
+      }
+    }
+    unpack8(k0v, k0f);
+    unpack8(k1v, k1f);
+    bool ok = true;
+    for (int pass = 0, lr0 = 0; lr0 < nrows; ++pass, lr0 += p.PR) {
+      const int n = nrows - lr0 < p.PR ? nrows - lr0 : p.PR;
+      const int mp = mb + lr0;
+      if (tid == 0 && ok) issue_pass(p, buf, &bars[0], mp, n, g0, cpy, l2_policy_evict_first());
+      if (tid < n)   // staged previous-tap row of row tid, or -1 for the row above
+        prev_off[tid] = (tid == 0 || (mp + tid) % p.L == 0) ? (p.PR + prev_index(mp, tid, p.L)) * rowb : -1;
+      ok = ok && mbar_wait_bounded(&bars[0], pass & 1, err);
+      __syncthreads();   // the pass's rows and the row table are in place
+      if (ok && active) {
+        uint4 carry = make_uint4(0, 0, 0, 0);
+        for (int jb = r0; jb < n; jb += 4 * R) {
+          uint4 xv[4], pv[4];
+          float c0[4], c1[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = jb + i * R;
+            if (j >= n) break;
+            xv[i] = reinterpret_cast<const uint4*>(buf + j * rowb)[u];
+            const int po = prev_off[j];
+            if (po >= 0)
+              pv[i] = reinterpret_cast<const uint4*>(buf + po)[u];
+            else if (R == 1)
+              pv[i] = i == 0 ? carry : xv[i - 1];
+            else
+              pv[i] = reinterpret_cast<const uint4*>(buf + (j - 1) * rowb)[u];
+            const float* srow = sums + (lr0 + j) * pitch;
+            c0[i] = srow[u >> 1] + b0;
+            c1[i] = srow[p.BNG + (u >> 1)] + b1;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = jb + i * R;
+            if (j >= n) break;
+            write8(p, mp + j, static_cast<int64_t>(g0) * 16 + u * 8, xv[i], pv[i], k0f, k1f, c0[i], c1[i]);
+            carry = xv[i];
+          }
+        }
+      }
+      __syncthreads();   // the buffer and the table are free again
     }
   }
 };
@@ -136,19 +220,37 @@ struct ConvEpi {
 cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* hs,
                             const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
-                            int y_is_fp32, uint32_t* err, cudaStream_t stream) {
+                            int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream) {
   const int64_t M = B * L;
   if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const int64_t G = d / 16;
+  const int G = static_cast<int>(d / 16);
+  int BNG = (G + 15) / 16 * 16;
+  if (BNG > kMaxGroupsPerTile) BNG = kMaxGroupsPerTile;
+  SplitKShape sh;
+  sh.M = static_cast<int>(M);
+  sh.K = static_cast<int>(d);
+  sh.BN = 2 * BNG;
+  sh.n_tiles = (G + BNG - 1) / BNG;
+  sh.m_tiles = static_cast<int>((M + 127) / 128);
+  sh.ks = sk_choose_ks(sh.n_tiles * sh.m_tiles, sh.K / kBK, num_sms);
+  sh.tmem_cols = 32;
+  while (sh.tmem_cols < static_cast<uint32_t>(sh.BN)) sh.tmem_cols <<= 1;
+  if (!sk_plan(sh)) return cudaErrorInvalidValue;
+  // the pass buffer follows the summed slot rows: PR x_t rows, then room for the
+  // staged previous-tap rows of any PR consecutive rows
+  const int stage_off = ((128 / sh.ks) * sk_partial_pitch(sh.BN) * 4 + 127) / 128 * 128;
+  const int rowb = BNG * 32;
+  const int Li = static_cast<int>(L < 128 ? L : 128);
+  int PR = 128 / sh.ks;
+  auto prevs = [&](int r) { const int c = 1 + (r - 1 + Li - 1) / Li; return c < r ? c : r; };
+  while (PR > 0 && (PR + prevs(PR)) * rowb > sh.region_bytes - kPrevTableBytes - stage_off) --PR;
+  if (PR < 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16_2d(&ta, hs ? hs : x, M, d, d, 128) ||
-      !make_tmap_bf16_2d(&tb, W_c, 2 * G, d, d, ConvEpi::kGroups))
+  if (!make_tmap_bf16_2d(&ta, hs ? hs : x, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_c, 2 * G, d, d, BNG))
     return cudaErrorInvalidValue;
   ConvEpi::Params p{x, x_prev, k0, k1, b_c, y, y_is_fp32, static_cast<int>(M), static_cast<int>(L),
-                    static_cast<int>(d), static_cast<int>(G)};
-  const int grid_n = static_cast<int>((G + ConvEpi::kGroups - 1) / ConvEpi::kGroups);
-  return launch_tc_gemm<ConvEpi::kBN, 3, ConvEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d), grid_n, p,
-                                                  err, stream);
+                    static_cast<int>(d), G, BNG, PR, stage_off};
+  return launch_splitk_gemm<ConvEpi>(ta, tb, sh, p, err, stream);
 }
 
 }  // namespace dflash2

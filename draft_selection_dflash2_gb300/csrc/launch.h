@@ -13,7 +13,7 @@ cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t
                         int32_t* idx, uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_H, int64_t M,
-                        int64_t d, float* gate, uint32_t* err, cudaStream_t stream);
+                        int64_t d, float* gate, uint32_t* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
                                const int32_t* last_verified, const float* gate, const uint16_t* A,
                                const uint16_t* Bt, int64_t B, int64_t L, int64_t V, float* S,
@@ -26,7 +26,7 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
 cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* hs,
                             const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
-                            int y_is_fp32, uint32_t* err, cudaStream_t stream);
+                            int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                           const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,

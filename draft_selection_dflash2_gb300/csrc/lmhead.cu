@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                   int64_t V, int d, int m_tiles, int n_tiles, int tiles_per_run, int n_runs,
                   uint64_t* __restrict__ partial, uint32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = align_smem<1024>(smem_raw);
   LmSmem& s = *reinterpret_cast<LmSmem*>(ring + kLmStages * kLmStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x % m_tiles;

@@ -3,8 +3,9 @@
 // S_t(a,b) = U_t(b) + <A(a) (.) H(h_t), B(b)>).
 //
 // gate             H = sigmoid(W_H h + b_H): one [B*L, d] x [d, 256] contraction on
-//                  the tensor cores (tcgen05 + TMA, fp32 in TMEM), sigmoid fused
-//                  in the epilogue.
+//                  the tensor cores (tcgen05 + TMA, fp32 in TMEM, K split over a
+//                  cluster and reduced in distributed shared memory), sigmoid
+//                  fused in the epilogue.
 // pair_kernel      one CTA per block position (b, t): gathers the 16 predecessor
 //                  rows of A and the 16 candidate rows of B (512 B each) with
 //                  16-byte loads, forms G = A_pred (.) H_t in fp32 shared memory,
@@ -12,15 +13,16 @@
 //                  tile per thread over 16 interleaved slices of r, reduced by a
 //                  15-shuffle reduce-scatter.
 #include "common.cuh"
-#include "gemm_tc.cuh"
+#include "gemm_splitk.cuh"
 #include "launch.h"
 
 namespace dflash2 {
 namespace {
 
 // ---------------------------------------------------------------------------
-// gate: H = sigmoid(h W_H^T + b) on the tensor cores (tcgen05, fp32 in TMEM),
-// 128 positions x 64 gate channels per CTA, sigmoid fused in the epilogue.
+// gate: H = sigmoid(h W_H^T + b) on the tensor cores (gemm_splitk.cuh): 128
+// positions x all 256 gate channels per tile, K split over a cluster, partial
+// sums reduced through distributed shared memory, sigmoid in the epilogue.
 // ---------------------------------------------------------------------------
 struct GateEpi {
   struct Params {
@@ -28,30 +30,30 @@ struct GateEpi {
     const float* bias;    // [256] or null
     int M;
   };
-  static constexpr int kBN = 64;
-  static constexpr int kSmemBytes = 0;
+  __host__ __device__ static int sub_n(int BN) { return BN; }
 
-  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, const Params&, uint64_t* bar,
+  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, int, const Params&, uint64_t* bar,
                                 uint64_t pol) {
-    tma_load_2d(dst, tm, k, blockIdx.y * kBN, bar, pol);
+    tma_load_2d(dst, tm, k, 0, bar, pol);
   }
-  __device__ static void consume(const Params& p, uint8_t*, int m0, int row_local, int c, const float (&v)[32]) {
-    const int row = m0 + row_local;
-    if (row >= p.M) return;
-    const int n0 = blockIdx.y * kBN + c * 32;
-    float4* dst = reinterpret_cast<float4*>(p.gate + static_cast<int64_t>(row) * kEmbed + n0);
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
+  __device__ static __forceinline__ void finish(const Params& p, const SplitKShape& sh, uint8_t* region, uint64_t*,
+                                                int m0, int, int rank, int tid, uint32_t*) {
+    const SkPartials parts(reinterpret_cast<const float*>(region), sh.ks, sk_partial_pitch(sh.BN));
+    const int rows_per = 128 / sh.ks;
+    const int r0 = rank * rows_per;
+    const int total = rows_per * (kEmbed / 4);
+    for (int e = tid; e < total; e += kSkThreads) {
+      const int lr = e / (kEmbed / 4), c4 = (e % (kEmbed / 4)) * 4;
+      const int m = m0 + r0 + lr;
+      if (m >= p.M) continue;
+      const float4 z = parts.sum4(lr, c4);
+      const float zz[4] = {z.x, z.y, z.z, z.w};
       float o[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float z = v[i + j] + (p.bias ? p.bias[n0 + i + j] : 0.0f);
-        o[j] = 1.0f / (1.0f + expf(-z));
-      }
-      dst[i / 4] = make_float4(o[0], o[1], o[2], o[3]);
+      for (int j = 0; j < 4; ++j) o[j] = 1.0f / (1.0f + expf(-(zz[j] + (p.bias ? p.bias[c4 + j] : 0.0f))));
+      *reinterpret_cast<float4*>(p.gate + static_cast<int64_t>(m) * kEmbed + c4) = make_float4(o[0], o[1], o[2], o[3]);
     }
   }
-  __device__ static void finish(const Params&, uint8_t*, int, int) {}
 };
 
 // ---------------------------------------------------------------------------
@@ -153,14 +155,22 @@ __global__ void __launch_bounds__(256) pair_kernel(const int32_t* __restrict__ c
 }  // namespace
 
 cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_H, int64_t M,
-                        int64_t d, float* gate, uint32_t* err, cudaStream_t stream) {
+                        int64_t d, float* gate, uint32_t* err, int num_sms, cudaStream_t stream) {
   if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  SplitKShape sh;
+  sh.M = static_cast<int>(M);
+  sh.K = static_cast<int>(d);
+  sh.BN = kEmbed;
+  sh.n_tiles = 1;
+  sh.m_tiles = static_cast<int>((M + 127) / 128);
+  sh.ks = sk_choose_ks(sh.m_tiles, sh.K / kBK, num_sms);
+  sh.tmem_cols = kEmbed;
+  if (!sk_plan(sh)) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16_2d(&ta, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_H, kEmbed, d, d, GateEpi::kBN))
+  if (!make_tmap_bf16_2d(&ta, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_H, kEmbed, d, d, kEmbed))
     return cudaErrorInvalidValue;
   GateEpi::Params p{gate, b_H, static_cast<int>(M)};
-  return launch_tc_gemm<GateEpi::kBN, 6, GateEpi>(ta, tb, static_cast<int>(M), static_cast<int>(d),
-                                                  kEmbed / GateEpi::kBN, p, err, stream);
+  return launch_splitk_gemm<GateEpi>(ta, tb, sh, p, err, stream);
 }
 
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,

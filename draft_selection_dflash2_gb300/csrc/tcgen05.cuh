@@ -38,6 +38,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Cluster barrier in two halves: every thread of every CTA of the cluster
+// arrives (release: its earlier shared/distributed-shared writes become visible)
+// and later waits (acquire) for all the others.  A thread alternates the two.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // UMMA descriptors
 // ---------------------------------------------------------------------------
