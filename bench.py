@@ -239,7 +239,8 @@ class Cycle:
         self.acc = [torch.empty((nb,), dtype=torch.int32, device=dev) for _ in range(2)]
         self.out = [torch.empty((nb, L + 1), dtype=torch.int32, device=dev) for _ in range(2)]
         self.target = None
-        self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 3)
+        # conv x10, top-16, gate + pairs, then per temperature: walk + verify (init + one cooperative kernel)
+        self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 2)
 
     def step(self, ev=None, seed_offset=0):
         api, h = self.api, self.h

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libdflash2: handle management, host-side argument
-// validation and dispatch to the kernels.  Nothing here allocates memory on the
-// compute path; the only allocation is the 4-byte device error word at create.
+// validation and dispatch to the kernels.  The handle owns two device buffers:
+// the 4-byte error word and the verification scratch (1 MiB at create, grown
+// by a verification call that needs more; see dflash2_verify).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -12,7 +13,9 @@
 struct dflash2_handle {
   int device = 0;
   int num_sms = 0;
-  uint32_t* err = nullptr;   // device error word
+  uint32_t* err = nullptr;      // device error word
+  void* scratch = nullptr;      // verification scratch
+  size_t scratch_bytes = 0;
 };
 
 namespace {
@@ -33,6 +36,31 @@ int launched(cudaError_t e) {
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 bool bad_handle(const dflash2_handle* h) { return h == nullptr || h->err == nullptr; }
+
+constexpr size_t kInitialScratch = size_t(1) << 20;
+
+// Grows the handle's scratch to at least `bytes`.  Growing allocates, which a
+// stream under graph capture cannot do: then the call fails with
+// DFLASH2_ERR_WORKSPACE and leaves the capture intact.
+int ensure_scratch(dflash2_handle* h, size_t bytes, cudaStream_t stream) {
+  if (h->scratch_bytes >= bytes) return DFLASH2_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return DFLASH2_ERR_WORKSPACE;
+  if (h->scratch) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return DFLASH2_ERR_CUDA;   // earlier calls may still use it
+    cudaFree(h->scratch);
+    h->scratch = nullptr;
+    h->scratch_bytes = 0;
+  }
+  size_t n = bytes < 2 * h->scratch_bytes ? 2 * h->scratch_bytes : bytes;
+  if (cudaMalloc(&h->scratch, n) != cudaSuccess) {
+    h->scratch = nullptr;
+    return DFLASH2_ERR_CUDA;
+  }
+  h->scratch_bytes = n;
+  return DFLASH2_OK;
+}
 
 }  // namespace
 
@@ -66,11 +94,14 @@ int dflash2_create(int device, dflash2_handle** out) {
   h->device = device;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       cudaMalloc(&h->err, sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess) {
+      cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&h->scratch, kInitialScratch) != cudaSuccess) {
     if (h->err) cudaFree(h->err);
+    if (h->scratch) cudaFree(h->scratch);
     delete h;
     return DFLASH2_ERR_CUDA;
   }
+  h->scratch_bytes = kInitialScratch;
   *out = h;
   return DFLASH2_OK;
 }
@@ -83,6 +114,7 @@ int dflash2_destroy(dflash2_handle* h) {
       st = DFLASH2_ERR_CUDA;
     cudaFree(h->err);
   }
+  if (h->scratch) cudaFree(h->scratch);
   delete h;
   return st;
 }
@@ -172,7 +204,7 @@ int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const 
                    int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,
                    uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* stream) {
   if (bad_handle(h) || B < 0 || L < 0 || V <= 0 || ld < V) return DFLASH2_ERR_INVALID_ARG;
-  if (L > kMaxL || V >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
+  if (L > kMaxL || V > dflash2::verify_max_vocab()) return DFLASH2_ERR_UNSUPPORTED;
   if (!(temperature == temperature)) return DFLASH2_ERR_INVALID_ARG;
   if (B == 0) return DFLASH2_OK;
   const bool sampled = temperature > 0.0f;
@@ -182,8 +214,10 @@ int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const 
       !aligned(out_tok, 4) || (draft_slot && !aligned(draft_slot, 4)) ||
       (draft_q && !aligned(draft_q, 4)) || (cand_idx && !aligned(cand_idx, 4)))
     return DFLASH2_ERR_MISALIGNED;
+  const int st = ensure_scratch(h, dflash2::verify_scratch_bytes(B, L, V), as_stream(stream));
+  if (st != DFLASH2_OK) return st;
   return launched(dflash2::launch_verify(target, ld, draft_tok, draft_slot, draft_q, cand_idx, B, L, V,
-                                         temperature, seed, offset, accept_len, out_tok, h->err,
+                                         temperature, seed, offset, accept_len, out_tok, h->scratch, h->err,
                                          h->num_sms, as_stream(stream)));
 }
 

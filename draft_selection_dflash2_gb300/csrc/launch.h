@@ -28,11 +28,17 @@ cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uin
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
                             int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream);
 
+// Device scratch (work queue, per-row arrival counters, per-chunk partials)
+// that launch_verify needs for B sequences of L positions over a V-id vocabulary.
+size_t verify_scratch_bytes(int64_t B, int64_t L, int64_t V);
+// Largest vocabulary launch_verify handles (10,485,760 ids).
+int64_t verify_max_vocab();
+
 cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                           const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
                           int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,
-                          uint64_t offset, int32_t* accept_len, int32_t* out_tok, uint32_t* err,
-                          int num_sms, cudaStream_t stream);
+                          uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* scratch,
+                          uint32_t* err, int num_sms, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms);
 constexpr size_t kLmheadNoAllocScratchBytes = DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES;

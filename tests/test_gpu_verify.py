@@ -6,6 +6,7 @@ T > 0: exact except sequences whose oracle decision margin is below 1e-4
 counted and must be rare.  Losslessness is checked statistically on V = 64."""
 import numpy as np
 import pytest
+import torch
 from scipy import stats
 
 import oracle
@@ -29,7 +30,7 @@ def excused(margin):
 
 def draft(seed, B, L, V, T):
     rng = np.random.default_rng(seed)
-    ci = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(L)]) for _ in range(B)])
+    ci = np.stack([np.stack([rng.choice(V, K, replace=V < K) for _ in range(L)]) for _ in range(B)])
     ci = ci.astype(np.int32)
     S = (rng.standard_normal((B, L, K, K)) * 2).astype(np.float32)
     tok, slot, q, _ = oracle.walk(S, ci, temperature=float(np.float32(T)), seed=seed)
@@ -48,7 +49,7 @@ def padded(target, V):
 
 
 @pytest.mark.parametrize("B,L,V", [(1, 8, 4096), (16, 16, 151936), (128, 16, 8200), (5, 1, 4099),
-                                   (9, 64, 1000)])
+                                   (9, 64, 1000), (3, 5, 17), (2, 3, 9)])
 def test_greedy_verify_exact(handle, B, L, V):
     tok, slot, q, ci = draft(B + L, B, L, V, 0.0)
     target = padded(synth.target_planted(B * 3 + L, tok, V, agree=0.85), V)
@@ -58,7 +59,8 @@ def test_greedy_verify_exact(handle, B, L, V):
 
 
 @pytest.mark.parametrize("T", [1.0, 0.7])
-@pytest.mark.parametrize("B,L,V,plant", [(64, 16, 8200, 12.0), (16, 16, 151936, 16.0), (40, 4, 4099, 6.0)])
+@pytest.mark.parametrize("B,L,V,plant", [(64, 16, 8200, 12.0), (16, 16, 151936, 16.0), (40, 4, 4099, 6.0),
+                                         (6, 5, 17, 2.0)])
 def test_sampled_verify_matches_oracle(handle, B, L, V, plant, T):
     tok, slot, q, ci = draft(B * 7 + L, B, L, V, T)
     target = padded(synth.target_planted(B + 1, tok, V, agree=0.85, plant=plant), V)
@@ -106,3 +108,34 @@ def test_greedy_mean_acceptance_closed_form_on_gpu(handle):
     a = host(acc)
     expect = 1.0 + sum(r**k for k in range(1, L + 1))
     assert abs(a.mean() - expect) < 4 * a.std() / np.sqrt(B)
+
+
+def test_verify_scratch_grows_outside_capture_only(handle):
+    """The per-row scratch lives in the handle: a call that fits runs inside a
+    CUDA graph capture, a call that would need a larger buffer is refused there
+    (DFLASH2_ERR_WORKSPACE) without breaking the capture, and the same call
+    grows the buffer outside capture."""
+    h = api.Handle(0)
+    small = dict(B=4, L=4, V=1000)
+    tok, slot, q, ci = draft(3, small["B"], small["L"], small["V"], 0.0)
+    target = synth.target_planted(4, tok, small["V"], agree=0.85)
+    big_B, big_L, big_V = 20000, 16, 8   # 340k rows: well past the initial 1 MiB
+    big_tok = np.zeros((big_B, big_L), np.int32)
+    big_target = np.zeros((big_B, big_L + 1, big_V), np.uint16)
+    tg, tk, btg, btk = bf(target), i32(tok), bf(big_target), i32(big_tok)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        api.verify(h, tg, tk, V=small["V"])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            acc, out = api.verify(h, tg, tk, V=small["V"])
+            with pytest.raises(api.Dflash2Error):
+                api.verify(h, btg, btk, V=big_V)
+        graph.replay()
+    torch.cuda.synchronize()
+    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci, V=small["V"])
+    assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
+    bacc, _ = api.verify(h, btg, btk, V=big_V)   # grows the scratch
+    assert (host(bacc) >= 1).all()
+    h.close()
