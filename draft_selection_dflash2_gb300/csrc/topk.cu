@@ -14,7 +14,9 @@
 //     candidate buffer.  A packed bf16x2 max over each lane's 8 logits against
 //     max(warp threshold, CTA-wide bound) rejects almost every vector; the rare
 //     survivors are turned into exact 64-bit keys (value, -id) out of line and
-//     folded into the warp's top-16 with bitonic merges.  After each fold the
+//     buffered; once a warp holds more than kFoldAt of them it folds them into
+//     its top-16 with bitonic merges (survivors appear in most iterations early
+//     in a row, so folding on every one would dominate).  After each fold the
 //     warp raises the CTA-wide bound (shared memory atomicMax): the CTA's 16th
 //     best is at least any warp's 16th best, so the bound is safe for all warps.
 //   * At the end the eight warp lists are merged, then the S CTA lists meet in
@@ -33,6 +35,7 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnroll = 8;                           // vectors in flight per lane
+constexpr int kCtasPerSm = 4;
 constexpr int kFoldAt = 32;                          // fold a warp buffer beyond this many
 constexpr int kWarpCap = kFoldAt + 32 * 8;           // + one vector from every lane
 constexpr int kSegQuantum = 8;                       // segments start on 16-byte boundaries
@@ -84,6 +87,18 @@ __device__ __forceinline__ bool vec_reaches(uint4 v, __nv_bfloat162 t2) {
   return __hge2_mask(__hmax2(__hmax2(a, b), __hmax2(c, d)), t2) != 0u;
 }
 
+// Bit k set iff element k of the vector compares >= t2 (NaN never does).
+__device__ __forceinline__ uint32_t elem_reach_mask(uint4 v, __nv_bfloat162 t2) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t r = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[q]), t2);
+    m |= ((r & 1u) | ((r >> 15) & 2u)) << (2 * q);
+  }
+  return m;
+}
+
 // Per-warp selection state; `top` is distributed (lane i < 16 holds the i-th
 // best key, lanes 16..31 hold 0), `thr` is warp-uniform.
 struct WarpSel {
@@ -120,7 +135,7 @@ __device__ __noinline__ void fold_warp(WarpSel& w, uint64_t* cand, int* wcount, 
   w.thr = own > g ? own : g;
 }
 
-__global__ void __launch_bounds__(kThreads, 4) topk16_kernel(const uint16_t* __restrict__ logits,
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint16_t* __restrict__ logits,
                                                           int64_t V, int64_t ld, int64_t seg_len,
                                                           float* __restrict__ vals,
                                                           int32_t* __restrict__ idx) {
@@ -175,11 +190,18 @@ __global__ void __launch_bounds__(kThreads, 4) topk16_kernel(const uint16_t* __r
     __syncthreads();
   }
   for (; vb < n_vecs; vb += stride * kUnroll) {
+    // every vector of this iteration exists for every lane (all but a row's last)
+    const bool whole = vb + (kUnroll - 1) * stride + 32 <= n_vecs;
     if (vb != static_cast<int64_t>(warp) * 32) {
+      const uint4* p = reinterpret_cast<const uint4*>(seg) + (vb + lane);
+      if (whole) {
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t vi = vb + u * stride + lane;
-        v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kUnroll; ++u) v[u] = ldg_stream(reinterpret_cast<const uint16_t*>(p + u * stride));
+      } else {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          v[u] = vb + u * stride + lane < n_vecs ? ldg_stream(reinterpret_cast<const uint16_t*>(p + u * stride))
+                                                 : make_uint4(0u, 0u, 0u, 0u);
       }
     }
     const uint64_t g = *reinterpret_cast<volatile unsigned long long*>(&s.gthr);
@@ -191,10 +213,32 @@ __global__ void __launch_bounds__(kThreads, 4) topk16_kernel(const uint16_t* __r
     uint32_t mask = 0u;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const bool real = vb + u * stride + lane < n_vecs;
+      const bool real = whole || vb + u * stride + lane < n_vecs;
       if (real && (thr_ord == 0u || vec_reaches(v[u], t2))) mask |= 1u << u;
     }
     if (__ballot_sync(0xFFFFFFFFu, mask != 0u) != 0u) {
+      if (__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(__popc(mask))) <= 32u) {
+        // the usual case: few flagged vectors, and the buffer (at most kFoldAt
+        // keys between entries) has room for all their keys; each lane keys only
+        // the elements that reach the threshold value
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          if ((mask >> u) & 1u) {
+            const uint4 x = v[u];
+            const uint32_t id0 = static_cast<uint32_t>(seg_begin + (vb + u * stride + lane) * 8);
+            uint32_t em = thr_ord == 0u ? 0xFFu : elem_reach_mask(x, t2);
+            while (em) {
+              const int k = __ffs(em) - 1;
+              em &= em - 1u;
+              const uint64_t key = make_key(lane_elem(x, k), id0 + k);
+              if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
+            }
+          }
+        }
+        __syncwarp();
+        if (*reinterpret_cast<volatile int*>(wcount) > kFoldAt) fold_warp(w, cand, wcount, &s.gthr, lane);
+        continue;
+      }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const bool f = (mask >> u) & 1u;
@@ -203,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 4) topk16_kernel(const uint16_t* __r
         __syncwarp();
         if (*reinterpret_cast<volatile int*>(wcount) > kFoldAt) fold_warp(w, cand, wcount, &s.gthr, lane);
       }
-      fold_warp(w, cand, wcount, &s.gthr, lane);
     }
   }
   // NaN logits need no extra pass: while the threshold is empty every real
