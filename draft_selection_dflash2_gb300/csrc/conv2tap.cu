@@ -80,35 +80,57 @@ struct ConvEpi {
     }
   }
 
-  // 8 bf16 values (one 16-byte vector) as floats
-  __device__ static __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      f[2 * q] = __uint_as_float(w[q] << 16);
-      f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
+  // Packed fp32 pairs (Blackwell's f32x2 arithmetic: two independent fp32
+  // operations per instruction, each rounded as the scalar one would be).
+  // Element 0 of a pair sits in the low 32 bits.
+  __device__ static __forceinline__ uint64_t pair(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(hi)) << 32 | __float_as_uint(lo);
+  }
+  __device__ static __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+  }
+  __device__ static __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+  }
+  __device__ static __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+  }
+  // one word of two bf16 values as a float pair
+  __device__ static __forceinline__ uint64_t unpack2(uint32_t w) {
+    return static_cast<uint64_t>(w & 0xFFFF0000u) << 32 | static_cast<uint64_t>(w << 16);
   }
 
-  // y[m, ch .. ch+8) from 8 channels of x_t, x_{t-1}, the unpacked k0, k1 and the
+  // y[m, ch .. ch+8) from 8 channels of x_t, x_{t-1}, the k0, k1 pairs and the
   // group's coefficients: (k0 + c0) x_t + (k1 + c1) x_{t-1}, in fp32.
   __device__ static __forceinline__ void write8(const Params& p, int64_t m, int64_t ch, uint4 xv, uint4 pv,
-                                                const float (&k0f)[8], const float (&k1f)[8], float c0, float c1) {
-    float xt[8], xp[8], out[8];
-    unpack8(xv, xt);
-    unpack8(pv, xp);
+                                                const uint64_t (&k0p)[4], const uint64_t (&k1p)[4], float c0,
+                                                float c1) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+    const uint64_t c0p = pair(c0, c0), c1p = pair(c1, c1);
+    uint64_t out[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out[i] = fmaf(k0f[i] + c0, xt[i], (k1f[i] + c1) * xp[i]);
+    for (int q = 0; q < 4; ++q)
+      out[q] = fma2(add2(k0p[q], c0p), unpack2(xw[q]), mul2(add2(k1p[q], c1p), unpack2(pw[q])));
     const int64_t o = m * p.d + ch;
     if (p.y_is_fp32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
-      dst[0] = make_float4(out[0], out[1], out[2], out[3]);
-      dst[1] = make_float4(out[4], out[5], out[6], out[7]);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.y) + o);
+      dst[0] = make_uint4(static_cast<uint32_t>(out[0]), static_cast<uint32_t>(out[0] >> 32),
+                          static_cast<uint32_t>(out[1]), static_cast<uint32_t>(out[1] >> 32));
+      dst[1] = make_uint4(static_cast<uint32_t>(out[2]), static_cast<uint32_t>(out[2] >> 32),
+                          static_cast<uint32_t>(out[3]), static_cast<uint32_t>(out[3] >> 32));
     } else {
       uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(out[2 * q], out[2 * q + 1]);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(out[q])),
+                                                        __uint_as_float(static_cast<uint32_t>(out[q] >> 32)));
         w[q] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.y) + o) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -160,7 +182,6 @@ struct ConvEpi {
     const int u = tid % nu, r0 = tid / nu;
     uint4 k0v = make_uint4(0, 0, 0, 0), k1v = k0v;
     float b0 = 0.0f, b1 = 0.0f;
-    float k0f[8], k1f[8];
     if (active) {
       k0v = __ldg(reinterpret_cast<const uint4*>(p.k0 + static_cast<int64_t>(g0) * 16) + u);
       k1v = __ldg(reinterpret_cast<const uint4*>(p.k1 + static_cast<int64_t>(g0) * 16) + u);
@@ -169,8 +190,8 @@ struct ConvEpi {
         b1 = p.b_c[p.G + g0 + (u >> 1)];
       }
     }
-    unpack8(k0v, k0f);
-    unpack8(k1v, k1f);
+    const uint64_t k0p[4] = {unpack2(k0v.x), unpack2(k0v.y), unpack2(k0v.z), unpack2(k0v.w)};
+    const uint64_t k1p[4] = {unpack2(k1v.x), unpack2(k1v.y), unpack2(k1v.z), unpack2(k1v.w)};
     bool ok = true;
     for (int pass = 0, lr0 = 0; lr0 < nrows; ++pass, lr0 += p.PR) {
       const int n = nrows - lr0 < p.PR ? nrows - lr0 : p.PR;
@@ -205,7 +226,7 @@ struct ConvEpi {
           for (int i = 0; i < 4; ++i) {
             const int j = jb + i * R;
             if (j >= n) break;
-            write8(p, mp + j, static_cast<int64_t>(g0) * 16 + u * 8, xv[i], pv[i], k0f, k1f, c0[i], c1[i]);
+            write8(p, mp + j, static_cast<int64_t>(g0) * 16 + u * 8, xv[i], pv[i], k0p, k1p, c0[i], c1[i]);
             carry = xv[i];
           }
         }
