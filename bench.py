@@ -85,21 +85,21 @@ _PROFILED = {
     "conv": ["conv2tap_B128_d5120.md"],
     "topk": ["topk16_B128_V151936.md"],
     "pairs": ["gate_gemm_B128_d5120.md", "pair_kernel_B128.md"],
-    "verify0": ["verify_rows_T0_B128.md"],
-    "verify1": ["verify_rows_T1_B128.md"],
+    "verify0": ["verify_kernel_T0_B128.md"],
+    "verify1": ["verify_kernel_T1_B128.md"],
     "walk1": ["walk_T1_B128.md"],
 }
 _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
     "conv2tap": ["conv2tap.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
-    "verify_rows": ["verify.cu", "common.cuh", "philox.cuh"],
+    "verify": ["verify.cu", "common.cuh", "philox.cuh"],
     "pair_scores": ["select.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "walk": ["walk.cu", "common.cuh", "philox.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
 }
 _PROFILE_SOURCES = {"conv2tap_B128_d5120.md": "conv2tap", "topk16_B128_V151936.md": "topk16",
                     "gate_gemm_B128_d5120.md": "pair_scores", "pair_kernel_B128.md": "pair_scores",
-                    "verify_rows_T0_B128.md": "verify_rows", "verify_rows_T1_B128.md": "verify_rows",
+                    "verify_kernel_T0_B128.md": "verify", "verify_kernel_T1_B128.md": "verify",
                     "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead"}
 
 
@@ -350,8 +350,8 @@ def run_gpu(args):
     dom = max(STAGES, key=lambda n: stage_ms[n])
     kernel_name = {"conv": "splitk_gemm_kernel<ConvEpi>", "topk": "topk16_kernel",
                    "pairs": "splitk_gemm_kernel<GateEpi> + pair_kernel",
-                   "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_rows_kernel",
-                   "verify1": "verify_rows_kernel"}[dom]
+                   "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_kernel",
+                   "verify1": "verify_kernel"}[dom]
     per_launch_ms = stage_ms[dom] / (CONV_APPS if dom == "conv" else 1)
     per_launch_bytes = stage_bytes[dom] / (CONV_APPS if dom == "conv" else 1)
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
