@@ -21,9 +21,13 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // gate: H = sigmoid(h W_H^T + b) on the tensor cores (gemm_splitk.cuh): 128
-// positions x all 256 gate channels per tile, K split over a cluster, partial
-// sums reduced through distributed shared memory, sigmoid in the epilogue.
+// positions x 128 of the 256 gate channels per tile, K split over a cluster of
+// up to 4 CTAs (small clusters place readily next to other kernels' CTAs),
+// partial sums reduced through distributed shared memory, sigmoid in the
+// epilogue.
 // ---------------------------------------------------------------------------
+constexpr int kGateBN = 128;
+
 struct GateEpi {
   struct Params {
     float* gate;          // [M, 256]
@@ -32,26 +36,28 @@ struct GateEpi {
   };
   __host__ __device__ static int sub_n(int BN) { return BN; }
 
-  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, int, const Params&, uint64_t* bar,
+  __device__ static void load_b(void* dst, const CUtensorMap* tm, int k, int n_tile, const Params&, uint64_t* bar,
                                 uint64_t pol) {
-    tma_load_2d(dst, tm, k, 0, bar, pol);
+    tma_load_2d(dst, tm, k, n_tile * kGateBN, bar, pol);
   }
   __device__ static __forceinline__ void finish(const Params& p, const SplitKShape& sh, uint8_t* region, uint64_t*,
-                                                int m0, int, int rank, int tid, uint32_t*) {
+                                                int m0, int n_tile, int rank, int tid, uint32_t*) {
     const SkPartials parts(reinterpret_cast<const float*>(region), sh.ks, sk_partial_pitch(sh.BN));
     const int rows_per = 128 / sh.ks;
     const int r0 = rank * rows_per;
-    const int total = rows_per * (kEmbed / 4);
+    const int c0 = n_tile * kGateBN;
+    const int total = rows_per * (kGateBN / 4);
     for (int e = tid; e < total; e += kSkThreads) {
-      const int lr = e / (kEmbed / 4), c4 = (e % (kEmbed / 4)) * 4;
+      const int lr = e / (kGateBN / 4), c4 = (e % (kGateBN / 4)) * 4;
       const int m = m0 + r0 + lr;
       if (m >= p.M) continue;
       const float4 z = parts.sum4(lr, c4);
       const float zz[4] = {z.x, z.y, z.z, z.w};
       float o[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[j] = 1.0f / (1.0f + expf(-(zz[j] + (p.bias ? p.bias[c4 + j] : 0.0f))));
-      *reinterpret_cast<float4*>(p.gate + static_cast<int64_t>(m) * kEmbed + c4) = make_float4(o[0], o[1], o[2], o[3]);
+      for (int j = 0; j < 4; ++j) o[j] = 1.0f / (1.0f + expf(-(zz[j] + (p.bias ? p.bias[c0 + c4 + j] : 0.0f))));
+      *reinterpret_cast<float4*>(p.gate + static_cast<int64_t>(m) * kEmbed + c0 + c4) =
+          make_float4(o[0], o[1], o[2], o[3]);
     }
   }
 };
@@ -160,14 +166,15 @@ cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_
   SplitKShape sh;
   sh.M = static_cast<int>(M);
   sh.K = static_cast<int>(d);
-  sh.BN = kEmbed;
-  sh.n_tiles = 1;
+  sh.BN = kGateBN;
+  sh.n_tiles = kEmbed / kGateBN;
   sh.m_tiles = static_cast<int>((M + 127) / 128);
-  sh.ks = sk_choose_ks(sh.m_tiles, sh.K / kBK, num_sms);
-  sh.tmem_cols = kEmbed;
+  sh.ks = sk_choose_ks(sh.n_tiles * sh.m_tiles, sh.K / kBK, num_sms);
+  if (sh.ks > 4) sh.ks = 4;
+  sh.tmem_cols = kGateBN;
   if (!sk_plan(sh)) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16_2d(&ta, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_H, kEmbed, d, d, kEmbed))
+  if (!make_tmap_bf16_2d(&ta, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W_H, kEmbed, d, d, kGateBN))
     return cudaErrorInvalidValue;
   GateEpi::Params p{gate, b_H, static_cast<int>(M)};
   return launch_splitk_gemm<GateEpi>(ta, tb, sh, p, err, stream);

@@ -4,9 +4,11 @@
 // the same scores).  This is the only sequential part of the draft-block head.
 //
 // One warp per sequence.  The warp first copies the sequence's whole score
-// block S[b] ([L, 16, 16] fp32, 1 KB per position) into shared memory with
-// 16-byte loads, so the L dependent steps run out of shared memory instead of
-// paying a global-memory round trip each.  Lane j (j < 16) owns successor slot j.
+// block S[b] ([L, 16, 16] fp32, 1 KB per position, 16-byte loads) and its
+// candidate ids ([L, 16] int32) into shared memory, and (sampled walk)
+// computes the L Philox uniforms in parallel, one step per lane, so the L
+// dependent steps touch neither global memory nor Philox.  Lane j (j < 16)
+// owns successor slot j.
 //   greedy : shuffle arg-max over (value, lowest slot).
 //   sampled: everything in fp32 (the draw is an integer decided by floating
 //            point): c = log2(e) / T, w_j = exp2_neg((S_j - max) * c), Z and the
@@ -42,8 +44,14 @@ __device__ __forceinline__ float exp2_neg(float x) {
   return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
 }
 
-constexpr int kWalkWarps = 2;            // sequences per CTA (2 x 64 KB at L = 64)
+constexpr int kWalkWarps = 2;            // sequences per CTA (2 x 69 KB at L = 64)
 constexpr int kMaxWalkL = 64;
+// shared memory per sequence: S[b], its candidate ids and its L uniforms, rounded
+// up to 4 floats so that every sequence's block (copied with 16-byte stores)
+// starts on a 16-byte boundary
+__host__ __device__ inline size_t walk_smem_floats(int64_t L) {
+  return (static_cast<size_t>(L) * (kTopK * kTopK + kTopK + 1) + 3) & ~size_t(3);
+}
 
 __global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand_idx, int64_t B,
@@ -54,11 +62,21 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t b = static_cast<int64_t>(blockIdx.x) * kWalkWarps + warp;
   if (b >= B) return;
-  float* sb = wsm + static_cast<size_t>(warp) * L * kTopK * kTopK;
-  const float4* src = reinterpret_cast<const float4*>(S + b * L * kTopK * kTopK);
-  float4* dst = reinterpret_cast<float4*>(sb);
-  const int n4 = static_cast<int>(L * kTopK * kTopK / 4);
-  for (int i = lane; i < n4; i += 32) dst[i] = src[i];
+  float* sb = wsm + static_cast<size_t>(warp) * walk_smem_floats(L);
+  int32_t* ids = reinterpret_cast<int32_t*>(sb + L * kTopK * kTopK);
+  float* us = sb + L * (kTopK * kTopK + kTopK);
+  {
+    const float4* src = reinterpret_cast<const float4*>(S + b * L * kTopK * kTopK);
+    float4* dst = reinterpret_cast<float4*>(sb);
+    const int n4 = static_cast<int>(L * kTopK * kTopK / 4);
+    for (int i = lane; i < n4; i += 32) dst[i] = src[i];
+    const int32_t* isrc = cand_idx + b * L * kTopK;   // 4-byte aligned only
+    for (int i = lane; i < L * kTopK; i += 32) ids[i] = isrc[i];
+    if (temperature > 0.0f)
+      for (int t = lane; t < L; t += 32)
+        us[t] = static_cast<float>(
+            philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset));
+  }
   __syncwarp();
 
   const int j = lane & (kTopK - 1);
@@ -94,9 +112,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
         Z = __fadd_rn(Z, __shfl_sync(0xFFFFFFFFu, w, i));
         cdf[i] = Z;
       }
-      const float u = static_cast<float>(
-          philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset));
-      const float target = __fmul_rn(u, Z);
+      const float target = __fmul_rn(us[t], Z);
       int pick = -1;
 #pragma unroll
       for (int i = kTopK - 1; i >= 0; --i)
@@ -114,7 +130,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     }
     if (lane == 0) {
       draft_slot[b * L + t] = chosen;
-      draft_tok[b * L + t] = cand_idx[(b * L + t) * kTopK + chosen];
+      draft_tok[b * L + t] = ids[t * kTopK + chosen];
     }
     prev = chosen;
   }
@@ -125,11 +141,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
 cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
                         int32_t* draft_slot, float* draft_q, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(kWalkWarps) * L * kTopK * kTopK * sizeof(float);
+  const size_t smem = static_cast<size_t>(kWalkWarps) * walk_smem_floats(L) * sizeof(float);
   static bool configured = false;
   if (!configured) {
     const cudaError_t e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kWalkWarps * kMaxWalkL * kTopK * kTopK * 4);
+                                               static_cast<int>(kWalkWarps * walk_smem_floats(kMaxWalkL) * 4));
     if (e != cudaSuccess) return e;
     configured = true;
   }
