@@ -51,6 +51,10 @@ def _load():
         lib.oracle_verify.restype = None
         lib.oracle_lmhead_topk.argtypes = [P, P, I64, I64, P, I64, I, P, P, I]
         lib.oracle_lmhead_topk.restype = None
+        lib.oracle_walk_viterbi.argtypes = [P, P, I64, I64, I64, P, P, P, I]
+        lib.oracle_walk_viterbi.restype = None
+        lib.oracle_selector_eval.argtypes = [P, P, I64, I64, I64, P, P, P]
+        lib.oracle_selector_eval.restype = None
         lib.oracle_threads.argtypes = [I]
         lib.oracle_threads.restype = I
         _lib = lib
@@ -143,6 +147,41 @@ def walk(S, cand_idx, temperature=0.0, seed=0, offset=0, nthreads=None):
     _load().oracle_walk(_p(Sf), _p(ci), B, L, K, float(temperature), seed, offset, _p(tok), _p(slot),
                         _p(q), _p(margin), nthreads or default_threads())
     return tok, slot, q, margin
+
+
+def walk_viterbi(S, cand_idx, nthreads=None):
+    """Exact best path over S f32 [B, L, K, K] (reading R15) -> (draft_tok, draft_slot, score [B])."""
+    Sf = _c(S, np.float32)
+    ci = _c(cand_idx, np.int32)
+    B, L, K, _ = Sf.shape
+    tok = np.zeros((B, L), np.int32)
+    slot = np.zeros((B, L), np.int32)
+    score = np.zeros((B,), np.float32)
+    _load().oracle_walk_viterbi(_p(Sf), _p(ci), B, L, K, _p(tok), _p(slot), _p(score), nthreads or default_threads())
+    return tok, slot, score
+
+
+def selector_eval(gt, cand_idx):
+    """Table 1 evaluation (reading R16): gt int32 [B, L], cand_idx int32 [B, L, K] ->
+    (accept1 [B], accept16 [B], counts int64 [L, 4] = (n1, hit1, n16, hit16) per position)."""
+    g = _c(gt, np.int32)
+    ci = _c(cand_idx, np.int32)
+    B, L, K = ci.shape
+    a1 = np.zeros((B,), np.int32)
+    a16 = np.zeros((B,), np.int32)
+    counts = np.zeros((L, 4), np.int64)
+    _load().oracle_selector_eval(_p(g), _p(ci), B, L, K, _p(a1), _p(a16), _p(counts))
+    return a1, a16, counts
+
+
+def closed_form_accept(recalls):
+    """Expected acceptance length 1 + sum_k prod_{t<=k} r_t for conditional per-position
+    acceptance rates r_t (Table 1's note: the verifier's next token is included)."""
+    total, prod = 1.0, 1.0
+    for r in recalls:
+        prod *= float(r)
+        total += prod
+    return total
 
 
 def conv2tap(x_bits, x_prev_bits, k0_bits, k1_bits, W_c_bits, b_c=None, h_bits=None, nthreads=None):

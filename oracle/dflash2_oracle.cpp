@@ -37,6 +37,17 @@
 //       proposal q = the walk's per-step 16-slot distribution (zero elsewhere).
 //   R8  Philox counter = (b, t | stream << 24, offset_lo, offset_hi),
 //       key = (seed_lo, seed_hi); a uniform is (x0 >> 8) * 2^-24.
+//   R15 exact best-path walk (the pages call pairwise scoring "the simplest
+//       selector" and leave more to explore): the slot path j_0..j_{L-1}
+//       maximising S[0][0][j_0] + sum_{t>=1} S[t][j_{t-1}][j_t], the sum taken
+//       left to right in fp32 (the precision the scores are stored in, so the
+//       integer path is decided in one precision); ties keep the lowest
+//       predecessor, then the lowest final slot.
+//   R16 selector evaluation (Table 1): recall at position t counts sequences
+//       whose earlier positions were all correct under the same rule (top-1
+//       equal to the true token, or the true token among the 16); the
+//       acceptance length of a rule is 1 + its number of leading correct
+//       positions (the verifier's next token included).
 
 #include <algorithm>
 #include <cmath>
@@ -511,6 +522,102 @@ void oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t V, in
       vals[i * k + j] = logit[order[j]];
       idx[i * k + j] = static_cast<int32_t>(order[j]);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exact best-path walk over the pair scores (reading R15).  The
+// max-sum (Viterbi) recurrence over the 16 slots of each position:
+//   V_0[j] = S[b][0][0][j]
+//   V_t[j] = max_i (V_{t-1}[i] + S[b][t][i][j]),  P_t[j] = the first i attaining it
+// then j_{L-1} = the first slot attaining max_j V_{L-1}[j] and j_{t-1} = P_t[j_t].
+// Every V is an fp32 sum formed left to right, as written.
+// S: [B, L, K, K] fp32; outputs draft_tok, draft_slot: [B, L]; score: [B] (the
+// best path's V) or null.
+// ---------------------------------------------------------------------------
+void oracle_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int64_t K,
+                         int32_t* draft_tok, int32_t* draft_slot, float* score, int nthreads) {
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
+  for (int64_t b = 0; b < B; ++b) {
+    std::vector<float> Vp(static_cast<size_t>(K)), Vn(static_cast<size_t>(K));
+    std::vector<int32_t> back(static_cast<size_t>(L * K), 0);
+    for (int64_t j = 0; j < K; ++j) Vp[j] = S[((b * L + 0) * K + 0) * K + j];
+    for (int64_t t = 1; t < L; ++t) {
+      for (int64_t j = 0; j < K; ++j) {
+        int64_t arg = 0;
+        float best = Vp[0] + S[((b * L + t) * K + 0) * K + j];
+        for (int64_t i = 1; i < K; ++i) {
+          const float v = Vp[i] + S[((b * L + t) * K + i) * K + j];
+          if (v > best) {
+            best = v;
+            arg = i;
+          }
+        }
+        Vn[j] = best;
+        back[t * K + j] = static_cast<int32_t>(arg);
+      }
+      Vp.swap(Vn);
+    }
+    int64_t j = 0;
+    for (int64_t k = 1; k < K; ++k)
+      if (Vp[k] > Vp[j]) j = k;
+    if (score) score[b] = Vp[j];
+    for (int64_t t = L - 1; t >= 0; --t) {
+      draft_slot[b * L + t] = static_cast<int32_t>(j);
+      draft_tok[b * L + t] = cand_idx[(b * L + t) * K + j];
+      if (t > 0) j = back[t * K + j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Selector evaluation, Table 1 ("The Right Tokens Are Already There"; reading
+// R16).  For sequence b with true tokens gt[b][0..L) and candidates
+// cand_idx[b][t][0..16) (value-descending, so slot 0 is the top-1):
+//   hit1[t]  = cand_idx[b][t][0] == gt[b][t]
+//   hit16[t] = gt[b][t] is one of cand_idx[b][t][0..16)
+// accept1[b]  = 1 + the number of leading t with hit1,
+// accept16[b] = 1 + the number of leading t with hit16 (an oracle selector
+// that always picks the right candidate when it is there).
+// counts [L, 4] (int64, accumulated over b): at position t, the number of
+// sequences whose positions before t all hit under the top-1 rule, how many of
+// those hit at t, and the same two for the top-16 rule; Recall@1[t] and
+// Recall@16[t] are the ratios.
+// ---------------------------------------------------------------------------
+void oracle_selector_eval(const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L, int64_t K,
+                          int32_t* accept1, int32_t* accept16, int64_t* counts) {
+  for (int64_t i = 0; i < L * 4; ++i) counts[i] = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    bool alive1 = true, alive16 = true;
+    int32_t n1 = 0, n16 = 0;
+    for (int64_t t = 0; t < L; ++t) {
+      const int32_t* c = cand_idx + (b * L + t) * K;
+      const int32_t g = gt[b * L + t];
+      const bool h1 = c[0] == g;
+      bool h16 = false;
+      for (int64_t j = 0; j < K; ++j)
+        if (c[j] == g) h16 = true;
+      if (alive1) {
+        counts[t * 4 + 0] += 1;
+        if (h1) {
+          counts[t * 4 + 1] += 1;
+          ++n1;
+        } else {
+          alive1 = false;
+        }
+      }
+      if (alive16) {
+        counts[t * 4 + 2] += 1;
+        if (h16) {
+          counts[t * 4 + 3] += 1;
+          ++n16;
+        } else {
+          alive16 = false;
+        }
+      }
+    }
+    accept1[b] = 1 + n1;
+    accept16[b] = 1 + n16;
   }
 }
 

@@ -1,0 +1,161 @@
+"""Pins of the oracle's next-row functions against what the pages and the
+mathematics fix, not against the oracle itself:
+  * the exact best-path walk (reading R15): exhaustive search over all 16^L
+    slot paths with the same fp32 left-to-right sums, a special case that
+    reduces to the greedy walk, a hand case where greedy is myopic, and the
+    invariant best >= greedy;
+  * the selector evaluation (reading R16): Table 1's printed acceptance
+    lengths through the closed form, hand cases, and planted data whose mean
+    acceptance lengths and conditional recalls match the closed form."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import read_golden_rows
+
+K = 16
+
+
+# ---------------------------------------------------------------------------
+# exact best path
+# ---------------------------------------------------------------------------
+def brute_best(S):
+    """All K^L paths of one sequence (S: [L, K, K] f32), sums in fp32 left to
+    right: (max score, list of every path attaining it)."""
+    L = S.shape[0]
+    acc = S[0, 0, :].astype(np.float32)                       # [K]: paths of length 1
+    for t in range(1, L):
+        acc = (acc[..., None] + S[t][(None,) * (t - 1) + (slice(None), slice(None))]).astype(np.float32)
+    best = acc.max()
+    return best, [tuple(int(x) for x in p) for p in np.argwhere(acc == best)]
+
+
+@pytest.mark.parametrize("L", [1, 2, 3])
+def test_viterbi_matches_exhaustive_search(L):
+    rng = np.random.default_rng(100 + L)
+    B = 24
+    S = rng.standard_normal((B, L, K, K)).astype(np.float32)
+    ci = rng.integers(0, 5000, (B, L, K)).astype(np.int32)
+    tok, slot, score = oracle.walk_viterbi(S, ci)
+    unique = 0
+    for b in range(B):
+        best, paths = brute_best(S[b])
+        assert score[b] == best
+        if len(paths) == 1:
+            unique += 1
+            assert tuple(slot[b]) == paths[0]
+        assert tuple(slot[b]) in paths
+        assert list(tok[b]) == [ci[b, t, slot[b, t]] for t in range(L)]
+    assert unique >= B - 2
+
+
+def test_viterbi_without_predecessor_dependence_is_the_greedy_walk():
+    # S[t][i][j] = u_t[j] for every i: the best path is the per-position arg-max
+    rng = np.random.default_rng(7)
+    B, L = 16, 12
+    u = rng.standard_normal((B, L, 1, K)).astype(np.float32)
+    S = np.broadcast_to(u, (B, L, K, K)).copy()
+    ci = rng.integers(0, 1000, (B, L, K)).astype(np.int32)
+    _, vslot, _ = oracle.walk_viterbi(S, ci)
+    _, gslot, _, _ = oracle.walk(S, ci, temperature=0.0)
+    assert np.array_equal(vslot, gslot)
+    assert np.array_equal(vslot, u[:, :, 0, :].argmax(-1))
+
+
+def test_viterbi_hand_case_where_greedy_is_myopic():
+    S = np.full((1, 2, K, K), -1.0, np.float32)
+    S[0, 0, 0, 0] = 1.0          # greedy takes slot 0 first ...
+    S[0, 0, 0, 1] = 0.9
+    S[0, 1, 0, :] = -10.0        # ... and then has nowhere good to go
+    S[0, 1, 1, 5] = 5.0          # the best path goes through slot 1 to slot 5
+    ci = np.arange(2 * K, dtype=np.int32).reshape(1, 2, K)
+    tok, slot, score = oracle.walk_viterbi(S, ci)
+    _, gslot, _, _ = oracle.walk(S, ci, temperature=0.0)
+    assert list(gslot[0]) == [0, 0]
+    assert list(slot[0]) == [1, 5] and list(tok[0]) == [1, K + 5]
+    assert score[0] == np.float32(np.float32(0.9) + np.float32(5.0))
+
+
+def test_viterbi_ties_take_the_lowest_slots():
+    S = np.zeros((1, 3, K, K), np.float32)     # every path scores 0
+    ci = np.zeros((1, 3, K), np.int32)
+    _, slot, score = oracle.walk_viterbi(S, ci)
+    assert list(slot[0]) == [0, 0, 0] and score[0] == 0.0
+
+
+def test_viterbi_score_is_at_least_the_greedy_path():
+    rng = np.random.default_rng(11)
+    B, L = 64, 16
+    S = (rng.standard_normal((B, L, K, K)) * 2).astype(np.float32)
+    ci = rng.integers(0, 1000, (B, L, K)).astype(np.int32)
+    _, _, vscore = oracle.walk_viterbi(S, ci)
+    _, gslot, _, _ = oracle.walk(S, ci, temperature=0.0)
+    for b in range(B):
+        g = np.float32(S[b, 0, 0, gslot[b, 0]])
+        for t in range(1, L):
+            g = np.float32(g + S[b, t, gslot[b, t - 1], gslot[b, t]])
+        assert vscore[b] >= g
+    assert (vscore > -np.inf).all()
+
+
+# ---------------------------------------------------------------------------
+# selector evaluation
+# ---------------------------------------------------------------------------
+def test_closed_form_accept_reproduces_table1():
+    for row in read_golden_rows("table1_recall.txt"):
+        r = [float(x) for x in row[1:8]]
+        printed = float(row[8])
+        al = oracle.closed_form_accept(r)
+        assert math.floor(al * 100) / 100 == printed   # printed truncated to 2 decimals
+
+
+def test_selector_eval_hand_cases():
+    L = 4
+    gt = np.array([[10, 11, 12, 13],      # top-1 everywhere
+                   [10, 11, 12, 13],      # in the 16 but never top-1
+                   [10, 11, 12, 13],      # top-1, top-1, absent, top-1
+                   [10, 11, 12, 13]], np.int32)
+    ci = np.full((4, L, K), 99, np.int32)
+    ci[:, :, 1:] = np.arange(200, 200 + K - 1)
+    ci[0, :, 0] = gt[0]
+    ci[1, :, 7] = gt[1]
+    ci[2, [0, 1, 3], 0] = gt[2, [0, 1, 3]]
+    a1, a16, counts = oracle.selector_eval(gt, ci)
+    assert list(a1) == [5, 1, 3, 1]
+    assert list(a16) == [5, 5, 3, 1]
+    # sequence 3 has no hits at all
+    assert list(counts[0]) == [4, 2, 4, 3]            # t=0: all alive; hits: seq 0 and 2 / 0, 1, 2
+    assert list(counts[1]) == [2, 2, 3, 3]
+    assert list(counts[2]) == [2, 1, 3, 2]
+    assert list(counts[3]) == [1, 1, 2, 2]
+
+
+def test_selector_eval_planted_matches_the_closed_form():
+    # Table 1's recalls planted independently per position: E[accept] = closed form,
+    # and each position's conditional hit ratio estimates its recall
+    rows = {row[0]: [float(x) for x in row[1:8]] for row in read_golden_rows("table1_recall.txt")}
+    r1, r16 = np.array(rows["recall@1"]), np.array(rows["recall@16"])
+    B, L = 20000, 7
+    rng = np.random.default_rng(3)
+    gt = rng.integers(0, 1 << 20, (B, L)).astype(np.int32)
+    ci = rng.integers(1 << 21, 1 << 22, (B, L, K)).astype(np.int32)   # never a true token
+    u = rng.random((B, L))
+    top = u < r1
+    inside = (~top) & (u < r16)
+    slot = rng.integers(1, K, (B, L))
+    bb, tt = np.nonzero(top)
+    ci[bb, tt, 0] = gt[bb, tt]
+    bb, tt = np.nonzero(inside)
+    ci[bb, tt, slot[bb, tt]] = gt[bb, tt]
+    a1, a16, counts = oracle.selector_eval(gt, ci)
+    for acc, r in ((a1, r1), (a16, r16)):
+        expect = oracle.closed_form_accept(r)
+        assert abs(acc.mean() - expect) < 4 * acc.std() / math.sqrt(B)
+    for t in range(L):
+        for n_col, h_col, r in ((0, 1, r1[t]), (2, 3, r16[t])):
+            n, h = counts[t, n_col], counts[t, h_col]
+            sd = math.sqrt(r * (1 - r) / n)
+            assert abs(h / n - r) < 4 * sd + 1e-9
