@@ -384,6 +384,8 @@ def run_gpu(args):
         line["e2e"] = run_e2e(torch, api, h, w, cyc, dev, args)
     if rank == 0 and args.lmhead:
         line["lmhead"] = run_lmhead(torch, api, h, dev, pk)
+    if rank == 0 and args.next:
+        line["next"] = run_next(torch, api, h, cyc, dev, pk)
     if rank == 0 and args.cpu_baseline and world == 1:
         line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=64)
     if rank == 0:
@@ -453,19 +455,8 @@ def run_lmhead(torch, api, h, dev, pk, M=1024):
     idx = torch.empty((M, K), dtype=torch.int32, device=dev)
     flops = 2.0 * M * V * D
 
-    def timed(fn, reps=5):
-        for _ in range(2):
-            fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+    def timed(fn):
+        return _timed(torch, fn)
 
     fused_ms = timed(lambda: api.lmhead_topk(h, hidden, W, vals=vals, idx=idx, workspace=ws))
     logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
@@ -478,6 +469,96 @@ def run_lmhead(torch, api, h, dev, pk, M=1024):
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
                          "peak_source": pk["source"] + " (bf16 burst, MEASURED_PEAKS.json)"}}
+
+
+def _timed(torch, fn, reps=5, warm=2):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def table1_recalls():
+    """Table 1's recall@1 / recall@16 per draft position, from the golden fixture."""
+    rows = {}
+    with open(os.path.join(ROOT, "tests", "golden", "table1_recall.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if parts and not line.startswith("#"):
+                rows[parts[0]] = [float(x) for x in parts[1:8]]
+    return rows["recall@1"], rows["recall@16"]
+
+
+def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
+    """The next rows, timed beside the step (not part of it).
+    viterbi: the exact best-path walk on the step's pair scores S [B, 16, 16, 16]
+      (L2 flushed before each launch), and at B = 65536 on N(0, 4) scores
+      (1 GiB of S: larger than L2).
+    selector_eval: the Table 1 evaluation over 2^21 sequences of 7 positions with
+      Table 1's recalls planted independently per position (0.9 GiB of candidate
+      ids: larger than L2)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(17)
+    out = {}
+    nb = cyc.nb
+    tok = torch.empty((nb, L), dtype=torch.int32, device=dev)
+    slot = torch.empty((nb, L), dtype=torch.int32, device=dev)
+    sc = torch.empty((nb,), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ci = cyc.idx.view(nb, L, K)
+    ms_small = _timed(torch, lambda: (flush.zero_(), api.walk_viterbi(h, cyc.S, ci, draft_tok=tok, draft_slot=slot,
+                                                                      score=sc)), reps=9)
+    ms_flush = _timed(torch, lambda: flush.zero_(), reps=9)
+    del flush
+    S = torch.randn((B_vit, L, K, K), generator=g, device=dev, dtype=torch.float32) * 2
+    cidx = torch.randint(0, V, (B_vit, L, K), generator=g, device=dev, dtype=torch.int32)
+    tok = torch.empty((B_vit, L), dtype=torch.int32, device=dev)
+    slot = torch.empty((B_vit, L), dtype=torch.int32, device=dev)
+    sc = torch.empty((B_vit,), dtype=torch.float32, device=dev)
+    ms = _timed(torch, lambda: api.walk_viterbi(h, S, cidx, draft_tok=tok, draft_slot=slot, score=sc))
+    nbytes = B_vit * L * (K * K * 4 + K * 4 + 8) + B_vit * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["viterbi"] = {"workload": f"B={nb} L={L} (the step's S, L2 flushed)",
+                      "us": round(max(ms_small - ms_flush, 0.0) * 1e3, 2),
+                      "throughput": {"workload": f"B={B_vit} L={L}", "ms": round(ms, 4),
+                                     "sequences_per_s": round(B_vit / (ms * 1e-3), 1),
+                                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                                                  "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4)}}}
+    del S, cidx, tok, slot, sc
+
+    r1, r16 = table1_recalls()
+    Le = len(r1)
+    gt = torch.randint(0, 1 << 20, (B_eval, Le), generator=g, device=dev, dtype=torch.int32)
+    cand = torch.randint(1 << 21, 1 << 22, (B_eval, Le, K), generator=g, device=dev, dtype=torch.int32)
+    u = torch.rand((B_eval, Le), generator=g, device=dev)
+    top = u < torch.tensor(r1, device=dev)
+    inside = (~top) & (u < torch.tensor(r16, device=dev))
+    pos = torch.randint(1, K, (B_eval, Le, 1), generator=g, device=dev)
+    cand[:, :, 0] = torch.where(top, gt, cand[:, :, 0])
+    cand.scatter_(2, pos, torch.where(inside, gt, cand.gather(2, pos).squeeze(2)).unsqueeze(2))
+    del u, top, inside, pos
+    a1 = torch.empty((B_eval,), dtype=torch.int32, device=dev)
+    a16 = torch.empty((B_eval,), dtype=torch.int32, device=dev)
+    counts = torch.empty((Le, 4), dtype=torch.int64, device=dev)
+    ms = _timed(torch, lambda: api.selector_eval(h, gt, cand, accept1=a1, accept16=a16, counts=counts))
+    nbytes = B_eval * Le * (K * 4 + 4) + B_eval * 8 + Le * 4 * 8
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["selector_eval"] = {"workload": f"B={B_eval} L={Le}, Table 1 recalls planted", "ms": round(ms, 4),
+                            "sequences_per_s": round(B_eval / (ms * 1e-3), 1),
+                            "mean_accept_top1": round(float(a1.double().mean()), 4),
+                            "mean_accept_top16_oracle": round(float(a16.double().mean()), 4),
+                            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4)}}
+    del gt, cand, a1, a16, counts
+    return out
 
 
 def run_e2e(torch, api, h, w, cyc, dev, args):
@@ -595,6 +676,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-lmhead", dest="lmhead", action="store_false")
+    ap.add_argument("--no-next", dest="next", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -30,6 +30,8 @@ SIGNATURES = {
     "dflash2_topk": (I32, [P, P, I64, I64, I64, I32, P, P, P]),
     "dflash2_pair_scores": (I32, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, P, P]),
     "dflash2_walk": (I32, [P, P, P, I64, I64, F32, U64, U64, P, P, P, P]),
+    "dflash2_walk_viterbi": (I32, [P, P, P, I64, I64, P, P, P, P]),
+    "dflash2_selector_eval": (I32, [P, P, P, I64, I64, P, P, P, P]),
     "dflash2_conv2tap": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, P, I32, P]),
     "dflash2_verify": (I32, [P, P, I64, P, P, P, P, I64, I64, I64, F32, U64, U64, P, P, P]),
     "dflash2_lmhead_topk_workspace": (SZ, [P, I64, I64, I64]),

@@ -146,6 +146,34 @@ def walk(h: Handle, S, cand_idx, temperature: float = 0.0, seed: int = 0, offset
     return draft_tok, draft_slot, draft_q
 
 
+def walk_viterbi(h: Handle, S, cand_idx, draft_tok=None, draft_slot=None, score=None, want_score: bool = True,
+                 stream=None):
+    """Exact best path -> (draft_tok int32 [B, L], draft_slot int32 [B, L], score fp32 [B] or None)."""
+    B, L = S.shape[0], S.shape[1]
+    dev = S.device
+    draft_tok = torch.empty((B, L), dtype=torch.int32, device=dev) if draft_tok is None else draft_tok
+    draft_slot = torch.empty((B, L), dtype=torch.int32, device=dev) if draft_slot is None else draft_slot
+    if score is None and want_score:
+        score = torch.empty((B,), dtype=torch.float32, device=dev)
+    _check(h._lib.dflash2_walk_viterbi(h.ptr, _ptr(S), _ptr(cand_idx), B, L, _ptr(draft_tok), _ptr(draft_slot),
+                                       _ptr(score), _stream(stream)),
+           "dflash2_walk_viterbi")
+    return draft_tok, draft_slot, score
+
+
+def selector_eval(h: Handle, gt, cand_idx, accept1=None, accept16=None, counts=None, stream=None):
+    """Table 1 evaluation -> (accept1 int32 [B], accept16 int32 [B], counts int64 [L, 4])."""
+    B, L = gt.shape
+    dev = gt.device
+    accept1 = torch.empty((B,), dtype=torch.int32, device=dev) if accept1 is None else accept1
+    accept16 = torch.empty((B,), dtype=torch.int32, device=dev) if accept16 is None else accept16
+    counts = torch.empty((L, 4), dtype=torch.int64, device=dev) if counts is None else counts
+    _check(h._lib.dflash2_selector_eval(h.ptr, _ptr(gt), _ptr(cand_idx), B, L, _ptr(accept1), _ptr(accept16),
+                                        _ptr(counts), _stream(stream)),
+           "dflash2_selector_eval")
+    return accept1, accept16, counts
+
+
 def conv2tap(h: Handle, x, x_prev, k0, k1, W_c, b_c=None, hs=None, y=None, y_fp32: bool = False,
              stream=None):
     """x [B, L, d] bf16 -> y [B, L, d] (bf16, or fp32 when y_fp32)."""

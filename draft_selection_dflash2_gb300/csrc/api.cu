@@ -184,6 +184,30 @@ int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int
                                        draft_slot, draft_q, as_stream(stream)));
 }
 
+int dflash2_walk_viterbi(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
+                         int32_t* draft_tok, int32_t* draft_slot, float* score, void* stream) {
+  if (bad_handle(h) || B < 0 || L < 0) return DFLASH2_ERR_INVALID_ARG;
+  if (L > kMaxL || B >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
+  if (B == 0 || L == 0) return DFLASH2_OK;
+  if (!S || !cand_idx || !draft_tok || !draft_slot) return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(S, 16) || !aligned(cand_idx, 4) || !aligned(draft_tok, 4) || !aligned(draft_slot, 4) ||
+      (score && !aligned(score, 4)))
+    return DFLASH2_ERR_MISALIGNED;
+  return launched(dflash2::launch_walk_viterbi(S, cand_idx, B, L, draft_tok, draft_slot, score, as_stream(stream)));
+}
+
+int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L,
+                          int32_t* accept1, int32_t* accept16, int64_t* counts, void* stream) {
+  if (bad_handle(h) || B < 0 || L < 0) return DFLASH2_ERR_INVALID_ARG;
+  if (L > kMaxL || B >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
+  if (L == 0) return DFLASH2_OK;
+  if (!counts || (B > 0 && (!gt || !cand_idx || !accept1 || !accept16))) return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(counts, 8) || (B > 0 && (!aligned(gt, 4) || !aligned(cand_idx, 4) || !aligned(accept1, 4) ||
+                                        !aligned(accept16, 4))))
+    return DFLASH2_ERR_MISALIGNED;
+  return launched(dflash2::launch_selector_eval(gt, cand_idx, B, L, accept1, accept16, counts, as_stream(stream)));
+}
+
 int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_prev,
                      const uint16_t* hs, const uint16_t* k0, const uint16_t* k1,
                      const uint16_t* W_c, const float* b_c, int64_t B, int64_t L, int64_t d,

@@ -28,6 +28,12 @@ cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uin
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
                             int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* draft_tok,
+                                int32_t* draft_slot, float* score, cudaStream_t stream);
+
+cudaError_t launch_selector_eval(const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* accept1,
+                                 int32_t* accept16, int64_t* counts, cudaStream_t stream);
+
 // Device scratch (work queue, per-row arrival counters, per-chunk partials)
 // that launch_verify needs for B sequences of L positions over a V-id vocabulary.
 size_t verify_scratch_bytes(int64_t B, int64_t L, int64_t V);

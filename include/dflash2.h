@@ -7,6 +7,8 @@
  *   dflash2_topk          top-16 candidates per block position
  *   dflash2_pair_scores   context gate + pairwise path-selector scores
  *   dflash2_walk          greedy or temperature-sampled walk over the scores
+ *   dflash2_walk_viterbi  exact best path over the same scores
+ *   dflash2_selector_eval Table 1's recall and acceptance-length evaluation
  *   dflash2_conv2tap      two-tap dynamic depthwise convolution
  *   dflash2_verify        block verification -> acceptance lengths
  *   dflash2_lmhead_topk   LM head GEMM with a streaming top-16 epilogue
@@ -15,7 +17,8 @@
  *   - Pointers marked "device" are CUDA device pointers on the handle's device;
  *     "host" pointers are ordinary host memory.  The caller owns every buffer:
  *     the library never frees a pointer or keeps one past the call, and no call
- *     on the compute path allocates memory.
+ *     on the compute path allocates memory, except dflash2_verify when it needs
+ *     more scratch than the handle holds (see there).
  *   - bf16 tensors are passed as `const uint16_t*` holding bf16 bit patterns.
  *   - Tensors are row-major and contiguous unless an explicit leading dimension
  *     (`ld`, in elements) is given.  bf16 base pointers must be 16-byte aligned
@@ -141,6 +144,39 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
 int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                  float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
                  int32_t* draft_slot, float* draft_q, void* stream);
+
+/*
+ * Exact best path over the same scores.  "A Lightweight Path Selector" calls
+ * pairwise scoring the simplest selector and leaves more to explore; this walk
+ * keeps the scores and replaces the myopic step by the max-sum path:
+ *   slots j_0..j_{L-1} maximising S[b,0,0,j_0] + sum_{t>=1} S[b,t,j_{t-1},j_t],
+ *   the sum formed left to right in fp32; ties keep the lowest predecessor,
+ *   then the lowest final slot.
+ *   S           device fp32 [B, L, 16, 16];  cand_idx device int32 [B, L, 16]
+ *   draft_tok, draft_slot  device int32 [B, L]
+ *   score       device fp32 [B] (the best path's score) or NULL
+ * L <= 64.  Same layout, alignment and error rules as dflash2_walk.
+ */
+int dflash2_walk_viterbi(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
+                         int32_t* draft_tok, int32_t* draft_slot, float* score, void* stream);
+
+/*
+ * Selector evaluation, Table 1 of "DFlash 2: Keep Drafting Parallel" ("The
+ * Right Tokens Are Already There"): given the true tokens and the per-position
+ * top-16 candidates (slot 0 = top-1), per sequence
+ *   accept1[b]  = 1 + the number of leading positions whose top-1 is the true token,
+ *   accept16[b] = 1 + the number of leading positions whose 16 candidates hold it
+ *                 (an oracle selector that always picks the right candidate),
+ * and per position counts[t] = (sequences whose earlier positions all hit under
+ * the top-1 rule, how many of them hit at t, the same two under the top-16
+ * rule), so Recall@1[t] = counts[t][1] / counts[t][0] and Recall@16[t] =
+ * counts[t][3] / counts[t][2] are Table 1's conditional recalls.
+ *   gt          device int32 [B, L];  cand_idx device int32 [B, L, 16]
+ *   accept1, accept16  device int32 [B];  counts device int64 [L, 4] (overwritten)
+ * L <= 64.  int32 pointers 4-byte aligned, counts 8-byte aligned.
+ */
+int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L,
+                          int32_t* accept1, int32_t* accept16, int64_t* counts, void* stream);
 
 /*
  * Two-tap dynamic depthwise convolution.  "A Lightweight Local Convolution":

@@ -150,7 +150,7 @@ def walk(S, cand_idx, temperature=0.0, seed=0, offset=0, nthreads=None):
 
 
 def walk_viterbi(S, cand_idx, nthreads=None):
-    """Exact best path over S f32 [B, L, K, K] (reading R15) -> (draft_tok, draft_slot, score [B])."""
+    """Exact best path over S f32 [B, L, K, K] (reading R17) -> (draft_tok, draft_slot, score [B])."""
     Sf = _c(S, np.float32)
     ci = _c(cand_idx, np.int32)
     B, L, K, _ = Sf.shape
@@ -162,7 +162,7 @@ def walk_viterbi(S, cand_idx, nthreads=None):
 
 
 def selector_eval(gt, cand_idx):
-    """Table 1 evaluation (reading R16): gt int32 [B, L], cand_idx int32 [B, L, K] ->
+    """Table 1 evaluation (reading R18): gt int32 [B, L], cand_idx int32 [B, L, K] ->
     (accept1 [B], accept16 [B], counts int64 [L, 4] = (n1, hit1, n16, hit16) per position)."""
     g = _c(gt, np.int32)
     ci = _c(cand_idx, np.int32)

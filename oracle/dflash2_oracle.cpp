@@ -37,13 +37,13 @@
 //       proposal q = the walk's per-step 16-slot distribution (zero elsewhere).
 //   R8  Philox counter = (b, t | stream << 24, offset_lo, offset_hi),
 //       key = (seed_lo, seed_hi); a uniform is (x0 >> 8) * 2^-24.
-//   R15 exact best-path walk (the pages call pairwise scoring "the simplest
+//   R17 exact best-path walk (the pages call pairwise scoring "the simplest
 //       selector" and leave more to explore): the slot path j_0..j_{L-1}
 //       maximising S[0][0][j_0] + sum_{t>=1} S[t][j_{t-1}][j_t], the sum taken
 //       left to right in fp32 (the precision the scores are stored in, so the
 //       integer path is decided in one precision); ties keep the lowest
 //       predecessor, then the lowest final slot.
-//   R16 selector evaluation (Table 1): recall at position t counts sequences
+//   R18 selector evaluation (Table 1): recall at position t counts sequences
 //       whose earlier positions were all correct under the same rule (top-1
 //       equal to the true token, or the true token among the 16); the
 //       acceptance length of a rule is 1 + its number of leading correct
@@ -526,7 +526,7 @@ void oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t V, in
 }
 
 // ---------------------------------------------------------------------------
-// Exact best-path walk over the pair scores (reading R15).  The
+// Exact best-path walk over the pair scores (reading R17).  The
 // max-sum (Viterbi) recurrence over the 16 slots of each position:
 //   V_0[j] = S[b][0][0][j]
 //   V_t[j] = max_i (V_{t-1}[i] + S[b][t][i][j]),  P_t[j] = the first i attaining it
@@ -572,7 +572,7 @@ void oracle_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int
 
 // ---------------------------------------------------------------------------
 // Selector evaluation, Table 1 ("The Right Tokens Are Already There"; reading
-// R16).  For sequence b with true tokens gt[b][0..L) and candidates
+// R18).  For sequence b with true tokens gt[b][0..L) and candidates
 // cand_idx[b][t][0..16) (value-descending, so slot 0 is the top-1):
 //   hit1[t]  = cand_idx[b][t][0] == gt[b][t]
 //   hit16[t] = gt[b][t] is one of cand_idx[b][t][0..16)

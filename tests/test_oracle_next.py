@@ -1,10 +1,10 @@
 """Pins of the oracle's next-row functions against what the pages and the
 mathematics fix, not against the oracle itself:
-  * the exact best-path walk (reading R15): exhaustive search over all 16^L
+  * the exact best-path walk (reading R17): exhaustive search over all 16^L
     slot paths with the same fp32 left-to-right sums, a special case that
     reduces to the greedy walk, a hand case where greedy is myopic, and the
     invariant best >= greedy;
-  * the selector evaluation (reading R16): Table 1's printed acceptance
+  * the selector evaluation (reading R18): Table 1's printed acceptance
     lengths through the closed form, hand cases, and planted data whose mean
     acceptance lengths and conditional recalls match the closed form."""
 import itertools
