@@ -96,11 +96,14 @@ _SOURCES = {
     "pair_scores": ["select.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "walk": ["walk.cu", "common.cuh", "philox.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
+    "viterbi": ["viterbi.cu", "common.cuh"],
+    "eval": ["eval.cu", "common.cuh"],
 }
 _PROFILE_SOURCES = {"conv2tap_B128_d5120.md": "conv2tap", "topk16_B128_V151936.md": "topk16",
                     "gate_gemm_B128_d5120.md": "pair_scores", "pair_kernel_B128.md": "pair_scores",
                     "verify_kernel_T0_B128.md": "verify", "verify_kernel_T1_B128.md": "verify",
-                    "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead"}
+                    "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead",
+                    "walk_viterbi_B16384.md": "viterbi", "selector_eval_B524288.md": "eval"}
 
 
 def _source_hash(kernel):
@@ -486,6 +489,13 @@ def _timed(torch, fn, reps=5, warm=2):
     return statistics.median(ts)
 
 
+def _scaled_traffic(name, factor):
+    """DRAM bytes of a smaller captured case scaled by the units processed (the
+    traffic of these streaming kernels grows in proportion), or None."""
+    t = profiled_traffic([name])
+    return None if t is None else int(t * factor)
+
+
 def table1_recalls():
     """Table 1's recall@1 / recall@16 per draft position, from the golden fixture."""
     rows = {}
@@ -531,8 +541,31 @@ def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
                       "throughput": {"workload": f"B={B_vit} L={L}", "ms": round(ms, 4),
                                      "sequences_per_s": round(B_vit / (ms * 1e-3), 1),
                                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
-                                                  "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4)}}}
+                                                  "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                                  "traffic": _scaled_traffic("walk_viterbi_B16384.md", B_vit / 16384),
+                                                  "alg_bytes_per_launch": nbytes}}}
     del S, cidx, tok, slot, sc
+
+    # acceptance of the best path vs the greedy walk through the T=0 verify, on
+    # planted pair scores (a true slot path with +3 sigma on its transitions) and
+    # a target whose arg-max is the true token at every position
+    Bc, Vc = 2048, 4096
+    S, ci, _, true_tok = synth.planted_path(23, Bc, L, Vc, mu=3.0)
+    dS, dci = to_dev(torch, S, dev), to_dev(torch, ci, dev)
+    dtg = to_dev(torch, synth.target_planted(24, true_tok, Vc, agree=1.0), dev)
+    gtok, gslot, gq = api.walk(h, dS, dci, temperature=0.0)
+    vtok, vslot, _ = api.walk_viterbi(h, dS, dci, want_score=False)
+    ag, _ = api.verify(h, dtg, gtok, gslot, gq, dci, temperature=0.0)
+    av, _ = api.verify(h, dtg, vtok, vslot, gq, dci, temperature=0.0)
+    walk_ms = _timed(torch, lambda: api.walk(h, dS, dci, temperature=0.0, draft_tok=gtok, draft_slot=gslot,
+                                             want_q=False))
+    vit_ms = _timed(torch, lambda: api.walk_viterbi(h, dS, dci, draft_tok=vtok, draft_slot=vslot,
+                                                    want_score=False))
+    out["viterbi_vs_greedy"] = {"workload": f"B={Bc} L={L} V={Vc}, planted path mu=3 sigma=1",
+                                "mean_accept_greedy": round(float(ag.double().mean()), 4),
+                                "mean_accept_best_path": round(float(av.double().mean()), 4),
+                                "greedy_walk_us": round(walk_ms * 1e3, 2), "best_path_us": round(vit_ms * 1e3, 2)}
+    del dS, dci, dtg
 
     r1, r16 = table1_recalls()
     Le = len(r1)
@@ -556,7 +589,9 @@ def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
                             "mean_accept_top1": round(float(a1.double().mean()), 4),
                             "mean_accept_top16_oracle": round(float(a16.double().mean()), 4),
                             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
-                                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4)}}
+                                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                         "traffic": _scaled_traffic("selector_eval_B524288.md", B_eval / 524288),
+                                         "alg_bytes_per_launch": nbytes}}
     del gt, cand, a1, a16, counts
     return out
 

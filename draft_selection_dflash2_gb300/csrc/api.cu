@@ -181,7 +181,7 @@ int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int
       (draft_q && !aligned(draft_q, 4)))
     return DFLASH2_ERR_MISALIGNED;
   return launched(dflash2::launch_walk(S, cand_idx, B, L, temperature, seed, offset, draft_tok,
-                                       draft_slot, draft_q, as_stream(stream)));
+                                       draft_slot, draft_q, h->err, as_stream(stream)));
 }
 
 int dflash2_walk_viterbi(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
@@ -193,7 +193,8 @@ int dflash2_walk_viterbi(dflash2_handle* h, const float* S, const int32_t* cand_
   if (!aligned(S, 16) || !aligned(cand_idx, 4) || !aligned(draft_tok, 4) || !aligned(draft_slot, 4) ||
       (score && !aligned(score, 4)))
     return DFLASH2_ERR_MISALIGNED;
-  return launched(dflash2::launch_walk_viterbi(S, cand_idx, B, L, draft_tok, draft_slot, score, as_stream(stream)));
+  return launched(dflash2::launch_walk_viterbi(S, cand_idx, B, L, draft_tok, draft_slot, score, h->err,
+                                                   as_stream(stream)));
 }
 
 int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L,
@@ -205,7 +206,8 @@ int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* c
   if (!aligned(counts, 8) || (B > 0 && (!aligned(gt, 4) || !aligned(cand_idx, 4) || !aligned(accept1, 4) ||
                                         !aligned(accept16, 4))))
     return DFLASH2_ERR_MISALIGNED;
-  return launched(dflash2::launch_selector_eval(gt, cand_idx, B, L, accept1, accept16, counts, as_stream(stream)));
+  return launched(dflash2::launch_selector_eval(gt, cand_idx, B, L, accept1, accept16, counts, h->num_sms,
+                                                    as_stream(stream)));
 }
 
 int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_prev,

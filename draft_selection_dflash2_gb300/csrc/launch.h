@@ -21,7 +21,7 @@ cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
 
 cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
-                        int32_t* draft_slot, float* draft_q, cudaStream_t stream);
+                        int32_t* draft_slot, float* draft_q, uint32_t* err, cudaStream_t stream);
 
 cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* hs,
                             const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
@@ -29,10 +29,10 @@ cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uin
                             int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* draft_tok,
-                                int32_t* draft_slot, float* score, cudaStream_t stream);
+                                int32_t* draft_slot, float* score, uint32_t* err, cudaStream_t stream);
 
 cudaError_t launch_selector_eval(const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* accept1,
-                                 int32_t* accept16, int64_t* counts, cudaStream_t stream);
+                                 int32_t* accept16, int64_t* counts, int num_sms, cudaStream_t stream);
 
 // Device scratch (work queue, per-row arrival counters, per-chunk partials)
 // that launch_verify needs for B sequences of L positions over a V-id vocabulary.

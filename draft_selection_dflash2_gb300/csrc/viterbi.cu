@@ -4,8 +4,9 @@
 // greedy walk.  Scores add in fp32 from left to right; ties go to the lowest
 // predecessor slot and, at the end, to the lowest final slot.
 //
-// One warp per sequence.  The warp copies S[b] ([L, 16, 16] fp32, 16-byte
-// loads) and its candidate ids into shared memory.  Lane j (j < 16) holds V[j],
+// One warp per sequence.  The warp copies S[b] ([L, 16, 16] fp32, one bulk
+// asynchronous copy completing on an mbarrier) and its candidate ids into
+// shared memory.  Lane j (j < 16) holds V[j],
 // the best score of a path ending in slot j; at each step it forms
 // V[i] + S[t][i][j] for i = 0..15 in order, keeps the first strict maximum, and
 // records that predecessor as a byte in shared memory.  Lane 0 then takes the
@@ -29,22 +30,33 @@ __host__ __device__ inline size_t viterbi_smem_floats(int64_t L) {
 __global__ void __launch_bounds__(kViterbiWarps * 32)
     walk_viterbi_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand_idx, int64_t B, int64_t L,
                         int32_t* __restrict__ draft_tok, int32_t* __restrict__ draft_slot,
-                        float* __restrict__ score) {
+                        float* __restrict__ score, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) float wsm[];
+  __shared__ uint64_t bars[kViterbiWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t b = static_cast<int64_t>(blockIdx.x) * kViterbiWarps + warp;
   if (b >= B) return;
   float* sb = wsm + static_cast<size_t>(warp) * viterbi_smem_floats(L);
   int32_t* ids = reinterpret_cast<int32_t*>(sb + L * kTopK * kTopK);
   uint8_t* back = reinterpret_cast<uint8_t*>(sb + L * (kTopK * kTopK + kTopK));
+  // S[b] arrives by one bulk copy while the lanes load the ids
+  uint64_t* bar = &bars[warp];
+  if (lane == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(L * kTopK * kTopK * sizeof(float));
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(sb, S + b * L * kTopK * kTopK, bytes, bar, l2_policy_evict_first());
+  }
   {
-    const float4* src = reinterpret_cast<const float4*>(S + b * L * kTopK * kTopK);
-    float4* dst = reinterpret_cast<float4*>(sb);
-    for (int i = lane; i < L * kTopK * kTopK / 4; i += 32) dst[i] = src[i];
     const int32_t* isrc = cand_idx + b * L * kTopK;   // 4-byte aligned only
     for (int i = lane; i < L * kTopK; i += 32) ids[i] = isrc[i];
   }
   __syncwarp();
+  if (!mbar_wait_bounded(bar, 0, err)) {
+    mbar_wait_bounded(bar, 0, err);   // give the copy one more limit to land, then leave
+    return;
+  }
   const int j = lane & (kTopK - 1);
   float V = sb[j];   // t = 0: row 0 (the last verified token)
   for (int64_t t = 1; t < L; ++t) {
@@ -87,7 +99,7 @@ __global__ void __launch_bounds__(kViterbiWarps * 32)
 }  // namespace
 
 cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* draft_tok,
-                                int32_t* draft_slot, float* score, cudaStream_t stream) {
+                                int32_t* draft_slot, float* score, uint32_t* err, cudaStream_t stream) {
   if (L > kViterbiMaxL) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(kViterbiWarps) * viterbi_smem_floats(L) * sizeof(float);
   static bool configured = false;
@@ -99,7 +111,8 @@ cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>((B + kViterbiWarps - 1) / kViterbiWarps);
-  walk_viterbi_kernel<<<grid, kViterbiWarps * 32, smem, stream>>>(S, cand_idx, B, L, draft_tok, draft_slot, score);
+  walk_viterbi_kernel<<<grid, kViterbiWarps * 32, smem, stream>>>(S, cand_idx, B, L, draft_tok, draft_slot, score,
+                                                                      err);
   return cudaGetLastError();
 }
 

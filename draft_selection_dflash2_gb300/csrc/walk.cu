@@ -4,8 +4,8 @@
 // the same scores).  This is the only sequential part of the draft-block head.
 //
 // One warp per sequence.  The warp first copies the sequence's whole score
-// block S[b] ([L, 16, 16] fp32, 1 KB per position, 16-byte loads) and its
-// candidate ids ([L, 16] int32) into shared memory, and (sampled walk)
+// block S[b] ([L, 16, 16] fp32, 1 KB per position, one bulk asynchronous copy
+// completing on an mbarrier) and its candidate ids ([L, 16] int32) into shared memory, and (sampled walk)
 // computes the L Philox uniforms in parallel, one step per lane, so the L
 // dependent steps touch neither global memory nor Philox.  Lane j (j < 16)
 // owns successor slot j.
@@ -57,19 +57,25 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     walk_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand_idx, int64_t B,
                 int64_t L, float temperature, uint64_t seed, uint64_t offset,
                 int32_t* __restrict__ draft_tok, int32_t* __restrict__ draft_slot,
-                float* __restrict__ draft_q) {
+                float* __restrict__ draft_q, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) float wsm[];
+  __shared__ uint64_t bars[kWalkWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t b = static_cast<int64_t>(blockIdx.x) * kWalkWarps + warp;
   if (b >= B) return;
   float* sb = wsm + static_cast<size_t>(warp) * walk_smem_floats(L);
   int32_t* ids = reinterpret_cast<int32_t*>(sb + L * kTopK * kTopK);
   float* us = sb + L * (kTopK * kTopK + kTopK);
+  // S[b] arrives by one bulk copy while the lanes load the ids and draw the uniforms
+  uint64_t* bar = &bars[warp];
+  if (lane == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(L * kTopK * kTopK * sizeof(float));
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(sb, S + b * L * kTopK * kTopK, bytes, bar, l2_policy_evict_first());
+  }
   {
-    const float4* src = reinterpret_cast<const float4*>(S + b * L * kTopK * kTopK);
-    float4* dst = reinterpret_cast<float4*>(sb);
-    const int n4 = static_cast<int>(L * kTopK * kTopK / 4);
-    for (int i = lane; i < n4; i += 32) dst[i] = src[i];
     const int32_t* isrc = cand_idx + b * L * kTopK;   // 4-byte aligned only
     for (int i = lane; i < L * kTopK; i += 32) ids[i] = isrc[i];
     if (temperature > 0.0f)
@@ -78,6 +84,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
             philox_uniform24(seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 0, offset));
   }
   __syncwarp();
+  if (!mbar_wait_bounded(bar, 0, err)) {
+    mbar_wait_bounded(bar, 0, err);   // give the copy one more limit to land, then leave
+    return;
+  }
 
   const int j = lane & (kTopK - 1);
   const float cinv = temperature > 0.0f ? __fdiv_rn(1.44269504f, temperature) : 0.0f;
@@ -140,7 +150,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
 
 cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
-                        int32_t* draft_slot, float* draft_q, cudaStream_t stream) {
+                        int32_t* draft_slot, float* draft_q, uint32_t* err, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kWalkWarps) * walk_smem_floats(L) * sizeof(float);
   static bool configured = false;
   if (!configured) {
@@ -151,7 +161,7 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
   }
   const unsigned grid = static_cast<unsigned>((B + kWalkWarps - 1) / kWalkWarps);
   walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, temperature,
-                                                       seed, offset, draft_tok, draft_slot, draft_q);
+                                                       seed, offset, draft_tok, draft_slot, draft_q, err);
   return cudaGetLastError();
 }
 

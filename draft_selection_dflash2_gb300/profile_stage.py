@@ -5,7 +5,10 @@ times, so that a profiler (ncu) can capture that stage's kernels alone.
   python -m draft_selection_dflash2_gb300.profile_stage --stage topk [--B 128] [--reps 3]
 
 Stages: topk, pairs (gate + pair scores), walk0, walk1, conv (one application),
-verify0, verify1, lmhead (M=1024 hidden rows against the full vocabulary).
+verify0, verify1, lmhead (M=1024 hidden rows against the full vocabulary),
+viterbi (the exact best-path walk on N(0, 4) scores of B sequences) and eval
+(the Table 1 selector evaluation of B sequences of 7 positions with uniform
+candidate ids and the true token in slot 0 of 80% of the rows).
 """
 import argparse
 import os
@@ -29,7 +32,8 @@ def main():
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--stage", required=True,
-                    choices=["topk", "pairs", "walk0", "walk1", "conv", "verify0", "verify1", "lmhead"])
+                    choices=["topk", "pairs", "walk0", "walk1", "conv", "verify0", "verify1", "lmhead",
+                             "viterbi", "eval"])
     ap.add_argument("--B", type=int, default=128)
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
@@ -72,6 +76,21 @@ def main():
         dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
         tok_d, slot_d, q_d, ci_d = dev(tok), dev(slot), dev(q), dev(ci)
         run = lambda: api.verify(h, target, tok_d, slot_d, q_d, ci_d, temperature=T, seed=1)  # noqa: E731
+    elif args.stage == "viterbi":
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        S = torch.randn((B, L, K, K), generator=g, device="cuda") * 2
+        ci = torch.randint(0, V, (B, L, K), generator=g, device="cuda", dtype=torch.int32)
+        run = lambda: api.walk_viterbi(h, S, ci)  # noqa: E731
+    elif args.stage == "eval":
+        g = torch.Generator(device="cuda")
+        g.manual_seed(6)
+        Le = 7
+        gt = torch.randint(0, V, (B, Le), generator=g, device="cuda", dtype=torch.int32)
+        cand = torch.randint(0, V, (B, Le, K), generator=g, device="cuda", dtype=torch.int32)
+        hit = torch.rand((B, Le), generator=g, device="cuda") < 0.8
+        cand[:, :, 0] = torch.where(hit, gt, cand[:, :, 0])
+        run = lambda: api.selector_eval(h, gt, cand)  # noqa: E731
     else:
         M = 1024
         hidden = bf(torch, synth.normal_bits(1, (M, D)))

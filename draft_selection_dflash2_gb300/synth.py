@@ -205,6 +205,30 @@ def target_planted(seed: int, draft_tok: np.ndarray, V: int, agree: float = 0.85
     return out
 
 
+def planted_path(seed: int, B: int, L: int, V: int, mu: float = 3.0, sigma: float = 1.0, K: int = 16):
+    """Pair scores with a planted true slot path, for comparing walks.
+
+    Per sequence: 16 distinct candidate ids per position (uniform in [0, V)),
+    a uniform true slot p_t per position, and S f32 [B, L, 16, 16] of
+    N(0, sigma^2) noise plus mu on the true transition: at t = 0 on column p_0
+    of every row (the rows of position 0 are equal), at t >= 1 on
+    (p_{t-1}, p_t).  Returns (S, cand_idx, true_slot, true_tok)."""
+    rng = np.random.default_rng(seed)
+    cand = np.empty((B, L, K), np.int32)
+    for b in range(B):
+        for t in range(L):
+            cand[b, t] = rng.choice(V, K, replace=V < K)
+    p = rng.integers(0, K, (B, L))
+    S = (rng.standard_normal((B, L, K, K), dtype=np.float32) * np.float32(sigma)).astype(np.float32)
+    S[:, 0] = S[:, 0, :1, :]
+    bb = np.arange(B)
+    S[bb, 0, :, p[:, 0]] += np.float32(mu)
+    for t in range(1, L):
+        S[bb, t, p[:, t - 1], p[:, t]] += np.float32(mu)
+    tok = np.take_along_axis(cand, p[:, :, None], axis=2)[:, :, 0]
+    return S, cand, p.astype(np.int32), tok.astype(np.int32)
+
+
 def target_noise(seed: int, B: int, L: int, V: int, std: float = 1.0) -> np.ndarray:
     """Unplanted target logits [B, L+1, V], N(0, std^2) bf16."""
     return _normal_bits(np.random.default_rng(seed), (B, L + 1, V), std=std)

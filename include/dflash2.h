@@ -133,13 +133,19 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
  * sampling draws from the same scores.  Step t reads row 0 of S[b,0] at t = 0
  * and row draft_slot[b,t-1] afterwards.
  *   temperature <= 0: slot = lowest j maximising the row; draft_q one-hot.
- *   temperature  > 0: w_j = exp((S_j - max S) / T) in fp64, Z summed in slot
- *     order, u = Philox4x32-10 uniform of counter (b, t | 0 << 24, offset_lo,
- *     offset_hi), key (seed_lo, seed_hi), u = (x0 >> 8) * 2^-24; slot = smallest j
- *     with u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.
- *   S          device fp32 [B, L, 16, 16];  cand_idx device int32 [B, L, 16]
+ *   temperature  > 0: every step in fp32 with correctly rounded operations:
+ *     w_j = 2^((S_j - max S) * (log2(e) / T)) (Cody-Waite reduction and a
+ *     degree-7 Taylor polynomial), Z summed in slot order, u = Philox4x32-10
+ *     uniform of counter (b, t | 0 << 24, offset_lo, offset_hi), key (seed_lo,
+ *     seed_hi), u = (x0 >> 8) * 2^-24; slot = smallest j with
+ *     u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.
+ *   S          device fp32 [B, L, 16, 16], 16-byte aligned (each sequence's
+ *              block is staged in shared memory by one bulk copy)
+ *   cand_idx   device int32 [B, L, 16]
  *   draft_tok  device int32 [B, L];  draft_slot device int32 [B, L]
  *   draft_q    device fp32 [B, L, 16] or NULL
+ * A staging copy that does not complete within the wait limit raises
+ * DFLASH2_DEVERR_TIMEOUT and leaves that sequence's outputs unwritten.
  */
 int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                  float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,

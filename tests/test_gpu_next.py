@@ -125,3 +125,23 @@ def test_selector_eval_unaligned_candidates(handle):
     o1, o16, ocounts = oracle.selector_eval(gt, ci)
     assert np.array_equal(host(a1), o1) and np.array_equal(host(a16), o16)
     assert np.array_equal(host(counts), ocounts)
+
+
+def test_best_path_vs_greedy_acceptance_on_planted_data(handle):
+    # both walks and the T=0 verify on the GPU give the oracle's acceptance lengths,
+    # and the best path accepts more than greedy on planted pair scores
+    B, L, V = 256, 16, 800
+    S, ci, _, true_tok = synth.planted_path(2, B, L, V, mu=3.0)
+    target = synth.target_planted(3, true_tok, V, agree=1.0)
+    dS, dci = f32(S), i32(ci)
+    dtg = torch.from_numpy(target.view(np.int16)).cuda().view(torch.bfloat16)
+    gtok, gslot, gq = api.walk(handle, dS, dci, temperature=0.0)
+    vtok, vslot, _ = api.walk_viterbi(handle, dS, dci)
+    ag, _ = api.verify(handle, dtg, gtok, gslot, gq, dci, temperature=0.0)
+    av, _ = api.verify(handle, dtg, vtok, vslot, gq, dci, temperature=0.0)
+    otok, oslot, oq, _ = oracle.walk(S, ci, temperature=0.0)
+    vt, vs, _ = oracle.walk_viterbi(S, ci)
+    oag, _, _ = oracle.verify(target, otok, oslot, oq, ci, temperature=0.0)
+    oav, _, _ = oracle.verify(target, vt, vs, oq, ci, temperature=0.0)
+    assert np.array_equal(host(ag), oag) and np.array_equal(host(av), oav)
+    assert host(av).mean() > host(ag).mean() + 0.5

@@ -159,3 +159,32 @@ def test_selector_eval_planted_matches_the_closed_form():
             n, h = counts[t, n_col], counts[t, h_col]
             sd = math.sqrt(r * (1 - r) / n)
             assert abs(h / n - r) < 4 * sd + 1e-9
+
+
+# ---------------------------------------------------------------------------
+# best path vs greedy on planted data (acceptance length through the T=0 verify)
+# ---------------------------------------------------------------------------
+def planted_acceptance(seed, B, L, V, mu, sigma=1.0):
+    from draft_selection_dflash2_gb300 import synth
+    S, ci, _, true_tok = synth.planted_path(seed, B, L, V, mu=mu, sigma=sigma)
+    target = synth.target_planted(seed + 1, true_tok, V, agree=1.0)
+    gtok, gslot, gq, _ = oracle.walk(S, ci, temperature=0.0)
+    vtok, vslot, _ = oracle.walk_viterbi(S, ci)
+    ag, _, _ = oracle.verify(target, gtok, gslot, gq, ci, temperature=0.0)
+    av, _, _ = oracle.verify(target, vtok, vslot, gq, ci, temperature=0.0)
+    lead = lambda tok: 1 + np.cumprod(tok == true_tok, axis=1).sum(axis=1)   # noqa: E731
+    return ag, av, lead(gtok), lead(vtok)
+
+
+def test_planted_path_without_noise_is_found_by_both_walks():
+    ag, av, lg, lv = planted_acceptance(1, 32, 12, 600, mu=5.0, sigma=0.0)
+    assert (ag == 13).all() and (av == 13).all()
+
+
+def test_best_path_accepts_more_than_greedy_on_planted_data():
+    # the verifier's acceptance equals 1 + the leading run of true tokens (the
+    # planted target's arg-max is the true token), for both walks; the best path
+    # uses later positions' evidence, so its mean acceptance is higher
+    ag, av, lg, lv = planted_acceptance(2, 256, 16, 800, mu=3.0)
+    assert np.array_equal(ag, lg) and np.array_equal(av, lv)
+    assert av.mean() > ag.mean() + 0.5
