@@ -43,6 +43,8 @@ def _load():
         lib.oracle_gate.restype = None
         lib.oracle_pair_scores.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P, I]
         lib.oracle_pair_scores.restype = I
+        lib.oracle_pair_scores_proj.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, P, I]
+        lib.oracle_pair_scores_proj.restype = I
         lib.oracle_walk.argtypes = [P, P, I64, I64, I64, D, U64, U64, P, P, P, P, I]
         lib.oracle_walk.restype = None
         lib.oracle_conv2tap.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, P, I]
@@ -132,6 +134,25 @@ def pair_scores(cand_idx, cand_val, last_verified, H, A_bits, B_bits, nthreads=N
     S = np.zeros((B, L, K, K), np.float64)
     bad = _load().oracle_pair_scores(_p(ci), _p(cv), _p(lv), _p(Hh), _p(A), _p(Bt), B, L, K, r, V,
                                      _p(S), nthreads or default_threads())
+    return S, bool(bad)
+
+
+def pair_scores_proj(cand_idx, cand_val, last_verified, H, E_bits, WA_bits, WB_bits, nthreads=None):
+    """Projection form (reading R19): cand_*: [B, L, K]; H: f64 [B, L, r]; E: uint16 [V, d];
+    W_A, W_B: uint16 [r, d] -> (S f64 [B, L, K, K], bad_id flag)."""
+    ci = _c(cand_idx, np.int32)
+    cv = _c(cand_val, np.float32)
+    lv = _c(last_verified, np.int32)
+    Hh = _c(H, np.float64)
+    E = _c(E_bits, np.uint16)
+    WA = _c(WA_bits, np.uint16)
+    WB = _c(WB_bits, np.uint16)
+    B, L, K = ci.shape
+    V, d = E.shape
+    r = WA.shape[0]
+    S = np.zeros((B, L, K, K), np.float64)
+    bad = _load().oracle_pair_scores_proj(_p(ci), _p(cv), _p(lv), _p(Hh), _p(E), _p(WA), _p(WB), B, L, K, r, V, d,
+                                          _p(S), nthreads or default_threads())
     return S, bool(bad)
 
 

@@ -43,6 +43,11 @@
 //       left to right in fp32 (the precision the scores are stored in, so the
 //       integer path is decided in one precision); ties keep the lowest
 //       predecessor, then the lowest final slot.
+//   R19 projection-form selector: A(a) = W_A E(a) and B(b) = W_B E(b), with E
+//       the shared [V, d] token embedding and W_A, W_B [256, d] (the form whose
+//       parameter count, 3 x 256 x d for W_A, W_B and W_H, matches the 2.0M
+//       the pages state at d = 2560).  The projections are exact sums, not
+//       rounded to bf16 (the tables of R10 are this form folded offline).
 //   R18 selector evaluation (Table 1): recall at position t counts sequences
 //       whose earlier positions were all correct under the same rule (top-1
 //       equal to the true token, or the true token among the 16); the
@@ -252,6 +257,53 @@ int oracle_pair_scores(const int32_t* cand_idx, const float* cand_val,
         }
         any_bad |= bad;
       }
+    }
+  }
+  return any_bad;
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2b, projection form (reading R19): the same score with the embeddings
+// projected on the fly from the shared token embedding,
+//   A(a)_q = sum_k W_A[q, k] E[a, k],   B(b)_q = sum_k W_B[q, k] E[b, k],
+//   S[b, t, i, j] = U_t(c_t[j]) + sum_q A(p_i)_q * H[b, t, q] * B(c_t[j])_q,
+// predecessors as in the table form.  E: [V, d] bf16; W_A, W_B: [r, d] bf16;
+// H: [B, L, r] double; S: [B, L, K, K] double.  Ids are clamped and reported
+// as in the table form.  Returns 1 if any id was out of range, else 0.
+// ---------------------------------------------------------------------------
+static void project_row(const uint16_t* E, const uint16_t* W, int64_t id, int64_t r, int64_t d, double* out) {
+  for (int64_t q = 0; q < r; ++q) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; ++k) acc += widen_bf16(W[q * d + k]) * widen_bf16(E[id * d + k]);
+    out[q] = acc;
+  }
+}
+
+int oracle_pair_scores_proj(const int32_t* cand_idx, const float* cand_val, const int32_t* last_verified,
+                            const double* H, const uint16_t* E, const uint16_t* W_A, const uint16_t* W_B,
+                            int64_t B, int64_t L, int64_t K, int64_t r, int64_t V, int64_t d, double* S,
+                            int nthreads) {
+  int any_bad = 0;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(threads_for(nthreads)) reduction(| : any_bad)
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t t = 0; t < L; ++t) {
+      int bad = 0;
+      std::vector<double> Ap(static_cast<size_t>(K * r)), Bc(static_cast<size_t>(K * r));
+      for (int64_t i = 0; i < K; ++i) {
+        int64_t pred = (t == 0) ? last_verified[b] : cand_idx[(b * L + t - 1) * K + i];
+        pred = clamp_id(pred, V, &bad);
+        project_row(E, W_A, pred, r, d, &Ap[i * r]);
+        const int64_t cur = clamp_id(cand_idx[(b * L + t) * K + i], V, &bad);
+        project_row(E, W_B, cur, r, d, &Bc[i * r]);
+      }
+      const double* Ht = H + (b * L + t) * r;
+      for (int64_t i = 0; i < K; ++i)
+        for (int64_t j = 0; j < K; ++j) {
+          double acc = 0.0;
+          for (int64_t q = 0; q < r; ++q) acc += Ap[i * r + q] * Ht[q] * Bc[j * r + q];
+          S[((b * L + t) * K + i) * K + j] = static_cast<double>(cand_val[(b * L + t) * K + j]) + acc;
+        }
+      any_bad |= bad;
     }
   }
   return any_bad;

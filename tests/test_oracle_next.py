@@ -188,3 +188,50 @@ def test_best_path_accepts_more_than_greedy_on_planted_data():
     ag, av, lg, lv = planted_acceptance(2, 256, 16, 800, mu=3.0)
     assert np.array_equal(ag, lg) and np.array_equal(av, lv)
     assert av.mean() > ag.mean() + 0.5
+
+
+# ---------------------------------------------------------------------------
+# projection-form selector (reading R19), pinned to the table form (already
+# pinned) through embeddings whose projections are exact
+# ---------------------------------------------------------------------------
+def _proj_case(seed, B, L, V, d, r=256):
+    from draft_selection_dflash2_gb300 import synth
+    rng = np.random.default_rng(seed)
+    ci = rng.integers(0, V, (B, L, K)).astype(np.int32)
+    cv = rng.standard_normal((B, L, K)).astype(np.float32)
+    lv = rng.integers(0, V, B).astype(np.int32)
+    H = rng.random((B, L, r))
+    return synth, rng, ci, cv, lv, H
+
+
+def test_projection_with_one_hot_embeddings_is_the_table_form():
+    # E(v) = e_v: A(v) = column v of W_A exactly, so the table A[v, q] = W_A[q, v]
+    B, L, V, d = 3, 5, 48, 64
+    synth, rng, ci, cv, lv, H = _proj_case(1, B, L, V, d)
+    E = np.zeros((V, d), np.uint16)
+    E[np.arange(V), np.arange(V)] = synth.bf16_bits(np.float32(1.0))
+    WA = synth.bf16_bits(rng.standard_normal((256, d)).astype(np.float32))
+    WB = synth.bf16_bits(rng.standard_normal((256, d)).astype(np.float32))
+    lv[1] = V + 7                                   # out of range: clamped and reported by both
+    S, bad = oracle.pair_scores_proj(ci, cv, lv, H, E, WA, WB)
+    St, bad_t = oracle.pair_scores(ci, cv, lv, H, np.ascontiguousarray(WA[:, :V].T),
+                                   np.ascontiguousarray(WB[:, :V].T))
+    assert bad and bad_t
+    assert np.allclose(S, St, rtol=1e-13, atol=1e-13)
+
+
+def test_projection_with_integer_embeddings_matches_exact_tables():
+    # entries in {-1, 0, 1}: E W^T is an exact integer table (numpy integer matmul)
+    B, L, V, d = 2, 4, 300, 64
+    synth, rng, ci, cv, lv, H = _proj_case(2, B, L, V, d)
+    Ei = rng.integers(-1, 2, (V, d))
+    WAi = rng.integers(-1, 2, (256, d))
+    WBi = rng.integers(-1, 2, (256, d))
+    bits = lambda a: synth.bf16_bits(a.astype(np.float32))          # noqa: E731
+    S, bad = oracle.pair_scores_proj(ci, cv, lv, H, bits(Ei), bits(WAi), bits(WBi))
+    St, _ = oracle.pair_scores(ci, cv, lv, H, bits(Ei @ WAi.T), bits(Ei @ WBi.T))
+    assert not bad
+    assert np.allclose(S, St, rtol=1e-13, atol=1e-12)
+    # a zero W_B removes the pair term: the scores are the candidate logits
+    S0, _ = oracle.pair_scores_proj(ci, cv, lv, H, bits(Ei), bits(WAi), bits(0 * WBi))
+    assert np.array_equal(S0, np.broadcast_to(cv[:, :, None, :], S0.shape).astype(np.float64))
