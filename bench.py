@@ -93,7 +93,8 @@ _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
     "conv2tap": ["conv2tap.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "verify": ["verify.cu", "common.cuh", "philox.cuh"],
-    "pair_scores": ["select.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
+    "pair_scores": ["select.cu", "pair_math.cuh", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
+    "proj": ["proj.cu", "pair_math.cuh", "tcgen05.cuh", "common.cuh"],
     "walk": ["walk.cu", "common.cuh", "philox.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
     "viterbi": ["viterbi.cu", "common.cuh"],
@@ -389,6 +390,7 @@ def run_gpu(args):
         line["lmhead"] = run_lmhead(torch, api, h, dev, pk)
     if rank == 0 and args.next:
         line["next"] = run_next(torch, api, h, cyc, dev, pk)
+        line["next"]["projection_selector"]["table_form_pairs_ms_in_step"] = stages["pairs"]["ms"]
     if rank == 0 and args.cpu_baseline and world == 1:
         line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=64)
     if rank == 0:
@@ -462,6 +464,9 @@ def run_lmhead(torch, api, h, dev, pk, M=1024):
         return _timed(torch, fn)
 
     fused_ms = timed(lambda: api.lmhead_topk(h, hidden, W, vals=vals, idx=idx, workspace=ws))
+    W_H = (torch.randn((R, D), generator=g, device=dev, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    gate = torch.empty((M, R), dtype=torch.float32, device=dev)
+    gate_ms = timed(lambda: api.lmhead_topk_gate(h, hidden, W, W_H, vals=vals, idx=idx, gate=gate, workspace=ws))
     logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
     unfused_ms = timed(lambda: (torch.matmul(hidden, W.t(), out=logits), api.topk(h, logits, vals=vals, idx=idx)))
     tf = flops / (fused_ms * 1e-3) / 1e12
@@ -469,6 +474,7 @@ def run_lmhead(torch, api, h, dev, pk, M=1024):
     return {"workload": f"fused LM-head top-16 M={M} d={D} V={V}", "fused_ms": round(fused_ms, 4),
             "traffic": profiled_traffic(["lmhead_M1024_V151936_d5120.md"]),
             "unfused_cublas_plus_topk_ms": round(unfused_ms, 4),
+            "with_gate_folded_ms": round(gate_ms, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
                          "peak_source": pk["source"] + " (bf16 burst, MEASURED_PEAKS.json)"}}
@@ -550,8 +556,8 @@ def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
     # planted pair scores (a true slot path with +3 sigma on its transitions) and
     # a target whose arg-max is the true token at every position
     Bc, Vc = 2048, 4096
-    S, ci, _, true_tok = synth.planted_path(23, Bc, L, Vc, mu=3.0)
-    dS, dci = to_dev(torch, S, dev), to_dev(torch, ci, dev)
+    S, pci, _, true_tok = synth.planted_path(23, Bc, L, Vc, mu=3.0)
+    dS, dci = to_dev(torch, S, dev), to_dev(torch, pci, dev)
     dtg = to_dev(torch, synth.target_planted(24, true_tok, Vc, agree=1.0), dev)
     gtok, gslot, gq = api.walk(h, dS, dci, temperature=0.0)
     vtok, vslot, _ = api.walk_viterbi(h, dS, dci, want_score=False)
@@ -566,6 +572,30 @@ def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
                                 "mean_accept_best_path": round(float(av.double().mean()), 4),
                                 "greedy_walk_us": round(walk_ms * 1e3, 2), "best_path_us": round(vit_ms * 1e3, 2)}
     del dS, dci, dtg
+
+    # projection-form selector: A, B projected from a shared [V, d] embedding for
+    # the step's own candidates and gate (L2 flushed before each call)
+    E = torch.randn((V, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    WA = (torch.randn((R, D), generator=g, device=dev, dtype=torch.float32) / D ** 0.5).to(torch.bfloat16)
+    WB = (torch.randn((R, D), generator=g, device=dev, dtype=torch.float32) / D ** 0.5).to(torch.bfloat16)
+    P = torch.empty((nb * L * K + nb, 2 * R), dtype=torch.float32, device=dev)
+    Sp = torch.empty((nb, L, K, K), dtype=torch.float32, device=dev)
+    cv = cyc.vals.view(nb, L, K)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ms_p = _timed(torch, lambda: (flush.zero_(), api.pair_scores_proj(h, ci, cv, cyc.lv, cyc.gate, E, WA, WB, P=P,
+                                                                      S=Sp)), reps=9)
+    ms_f = _timed(torch, lambda: flush.zero_(), reps=9)
+    ms_p = max(ms_p - ms_f, 1e-6)
+    del flush, E
+    flops = (nb * L * K + nb) * 2 * R * D * 2.0
+    tf = flops / (ms_p * 1e-3) / 1e12
+    out["projection_selector"] = {
+        "workload": f"B={nb} L={L} V={V} d={D}: projections of {nb * L * K + nb} tokens + pair scores",
+        "ms": round(ms_p, 4), "table_form_pairs_ms_in_step": None,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / pk["bf16_tflops"], 4),
+                     "note": "whole call (projection GEMM + pair kernel) against the projection's flops"}}
+    del P, Sp, WA, WB
 
     r1, r16 = table1_recalls()
     Le = len(r1)

@@ -36,6 +36,9 @@ SIGNATURES = {
     "dflash2_verify": (I32, [P, P, I64, P, P, P, P, I64, I64, I64, F32, U64, U64, P, P, P]),
     "dflash2_lmhead_topk_workspace": (SZ, [P, I64, I64, I64]),
     "dflash2_lmhead_topk": (I32, [P, P, P, I64, I64, I64, P, P, P, SZ, P]),
+    "dflash2_lmhead_topk_gate": (I32, [P, P, P, P, P, I64, I64, I64, P, P, P, P, SZ, P]),
+    "dflash2_pair_scores_proj_workspace": (SZ, [P, I64, I64]),
+    "dflash2_pair_scores_proj": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, SZ, P, P]),
     "dflash2_lmhead_topk_noalloc": (I32, [P, P, P, I64, I64, I64, P, P, P]),
 }
 

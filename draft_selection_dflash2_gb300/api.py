@@ -224,6 +224,47 @@ def lmhead_topk(h: Handle, hidden, W, vals=None, idx=None, workspace=None, strea
     return vals, idx
 
 
+def lmhead_topk_gate(h: Handle, hidden, W, W_H, b_H=None, vals=None, idx=None, gate=None, workspace=None,
+                     stream=None):
+    """Fused LM head + top-16 + context gate -> (vals fp32 [M, 16], idx int32 [M, 16], gate fp32 [M, 256])."""
+    for name, t in (("hidden", hidden), ("W", W), ("W_H", W_H)):
+        _need(_is16(t) and t.is_contiguous(), f"{name}: contiguous bf16")
+    M, d = hidden.shape
+    V = W.shape[0]
+    dev = hidden.device
+    vals = torch.empty((M, K), dtype=torch.float32, device=dev) if vals is None else vals
+    idx = torch.empty((M, K), dtype=torch.int32, device=dev) if idx is None else idx
+    gate = torch.empty((M, EMBED), dtype=torch.float32, device=dev) if gate is None else gate
+    if workspace is None:
+        workspace = torch.empty(max(lmhead_topk_workspace(h, M, V, d), 256), dtype=torch.uint8, device=dev)
+    _check(h._lib.dflash2_lmhead_topk_gate(h.ptr, _ptr(hidden), _ptr(W), _ptr(W_H), _ptr(b_H), M, V, d, _ptr(vals),
+                                           _ptr(idx), _ptr(gate), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)), "dflash2_lmhead_topk_gate")
+    return vals, idx, gate
+
+
+def pair_scores_proj_workspace(h: Handle, B: int, L: int) -> int:
+    return h._lib.dflash2_pair_scores_proj_workspace(h.ptr, B, L)
+
+
+def pair_scores_proj(h: Handle, cand_idx, cand_val, last_verified, gate, E, W_A, W_B, P=None, S=None, stream=None):
+    """Projection-form pair scores -> (S fp32 [B, L, 16, 16], P fp32 [B*L*16 + B, 512])."""
+    B, L, k = cand_idx.shape
+    _need(k == K, "cand_idx: [B, L, 16]")
+    for name, t in (("E", E), ("W_A", W_A), ("W_B", W_B)):
+        _need(_is16(t) and t.is_contiguous(), f"{name}: contiguous bf16")
+    V, d = E.shape
+    dev = cand_idx.device
+    if P is None:
+        P = torch.empty((B * L * K + B, 2 * EMBED), dtype=torch.float32, device=dev)
+    S = torch.empty((B, L, K, K), dtype=torch.float32, device=dev) if S is None else S
+    _check(h._lib.dflash2_pair_scores_proj(h.ptr, _ptr(cand_idx), _ptr(cand_val), _ptr(last_verified), _ptr(gate),
+                                           _ptr(E), _ptr(W_A), _ptr(W_B), B, L, d, V, _ptr(P),
+                                           P.numel() * P.element_size(), _ptr(S), _stream(stream)),
+           "dflash2_pair_scores_proj")
+    return S, P
+
+
 def lmhead_topk_noalloc(h: Handle, hidden, W, vals=None, idx=None, stream=None):
     """lmhead_topk for callers that cannot allocate: the library's fixed
     device scratch replaces the workspace (calls sharing a device must not

@@ -268,6 +268,45 @@ int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_
                                               h->err, as_stream(stream)));
 }
 
+int dflash2_lmhead_topk_gate(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H,
+                             const float* b_H, int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx,
+                             float* gate, void* workspace, size_t ws_bytes, void* stream) {
+  if (bad_handle(h) || M < 0 || V < 0 || d <= 0) return DFLASH2_ERR_INVALID_ARG;
+  if (d % 64 != 0 || V < kK || V >= (int64_t(1) << 31) - 256) return DFLASH2_ERR_UNSUPPORTED;
+  if (M == 0) return DFLASH2_OK;
+  if (!hidden || !W || !W_H || !vals || !idx || !gate) return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(W_H, 16) || !aligned(vals, 4) || !aligned(idx, 4) ||
+      !aligned(gate, 16) || (b_H && !aligned(b_H, 4)) || (workspace && !aligned(workspace, 256)))
+    return DFLASH2_ERR_MISALIGNED;
+  if (workspace == nullptr || ws_bytes < dflash2::lmhead_workspace_bytes(M, V, d, h->num_sms))
+    return DFLASH2_ERR_WORKSPACE;
+  return launched(dflash2::launch_lmhead_topk_gate(hidden, W, W_H, b_H, M, V, d, vals, idx, gate, workspace,
+                                                   h->num_sms, h->err, as_stream(stream)));
+}
+
+size_t dflash2_pair_scores_proj_workspace(const dflash2_handle* h, int64_t B, int64_t L) {
+  if (bad_handle(h) || B <= 0 || L <= 0 || L > kMaxL) return 0;
+  return dflash2::proj_workspace_bytes(B, L);
+}
+
+int dflash2_pair_scores_proj(dflash2_handle* h, const int32_t* cand_idx, const float* cand_val,
+                             const int32_t* last_verified, const float* gate, const uint16_t* E,
+                             const uint16_t* W_A, const uint16_t* W_B, int64_t B, int64_t L, int64_t d, int64_t V,
+                             float* P, size_t P_bytes, float* S, void* stream) {
+  if (bad_handle(h) || B < 0 || L < 0 || d <= 0 || V <= 0) return DFLASH2_ERR_INVALID_ARG;
+  if (d % 64 != 0 || L > kMaxL || V >= (int64_t(1) << 31) || B * L >= (int64_t(1) << 26))
+    return DFLASH2_ERR_UNSUPPORTED;
+  if (B == 0 || L == 0) return DFLASH2_OK;
+  if (!cand_idx || !cand_val || !last_verified || !gate || !E || !W_A || !W_B || !P || !S)
+    return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(cand_idx, 4) || !aligned(cand_val, 4) || !aligned(last_verified, 4) || !aligned(gate, 16) ||
+      !aligned(E, 16) || !aligned(W_A, 16) || !aligned(W_B, 16) || !aligned(P, 16) || !aligned(S, 4))
+    return DFLASH2_ERR_MISALIGNED;
+  if (P_bytes < dflash2::proj_workspace_bytes(B, L)) return DFLASH2_ERR_WORKSPACE;
+  return launched(dflash2::launch_pair_scores_proj(cand_idx, cand_val, last_verified, gate, E, W_A, W_B, B, L, d,
+                                                   V, P, S, h->num_sms, h->err, as_stream(stream)));
+}
+
 int dflash2_lmhead_topk_noalloc(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
                                 int64_t V, int64_t d, float* vals, int32_t* idx, void* stream) {
   if (bad_handle(h) || M < 0 || V < 0 || d <= 0) return DFLASH2_ERR_INVALID_ARG;

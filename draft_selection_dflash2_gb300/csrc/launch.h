@@ -47,6 +47,18 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
                           uint32_t* err, int num_sms, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms);
+cudaError_t launch_lmhead_topk_gate(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H,
+                                    const float* b_H, int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx,
+                                    float* gate, void* workspace, int num_sms, uint32_t* err, cudaStream_t stream);
+
+// Projection-form pair scores: P = [W_A E(id); W_B E(id)] for the step's
+// candidates and last verified tokens, then S from P (proj.cu).
+size_t proj_rows(int64_t B, int64_t L);
+size_t proj_workspace_bytes(int64_t B, int64_t L);
+cudaError_t launch_pair_scores_proj(const int32_t* cand_idx, const float* cand_val, const int32_t* last_verified,
+                                    const float* gate, const uint16_t* E, const uint16_t* W_A, const uint16_t* W_B,
+                                    int64_t B, int64_t L, int64_t d, int64_t V, float* P, float* S, int num_sms,
+                                    uint32_t* err, cudaStream_t stream);
 constexpr size_t kLmheadNoAllocScratchBytes = DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES;
 cudaError_t lmhead_noalloc_scratch(int device, void** ptr);
 cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,

@@ -21,6 +21,9 @@
 //               the epilogue of tile i overlaps the MMAs of tile i + 1.
 //   At the end each thread writes its list as 16 order-preserving 64-bit keys
 //   (fp32 value, -id) to the workspace [M, n_runs, 16].
+//   With the context gate folded in, W_H's 256 rows are one more "vocabulary"
+//   tile after the last (0.17% more products at V = 151936): its epilogue
+//   writes H = sigmoid(acc + b_H) for the tile's rows instead of ranking them.
 // lmhead_merge_kernel: one warp per row folds the n_runs partial lists into the
 // final top-16 (value descending, lowest id on ties).
 #include <mutex>
@@ -67,9 +70,10 @@ __device__ __forceinline__ float logit_key_value(uint64_t k) {
 }
 
 __global__ void __launch_bounds__(kLmThreads, 1)
-    lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                  int64_t V, int d, int m_tiles, int n_tiles, int tiles_per_run, int n_runs,
-                  uint64_t* __restrict__ partial, uint32_t* __restrict__ err) {
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmH, int M, int64_t V, int d, int m_tiles, int n_tiles,
+                  int n_vocab_tiles, int tiles_per_run, int n_runs, uint64_t* __restrict__ partial,
+                  float* __restrict__ gate, const float* __restrict__ b_H, uint32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = align_smem<1024>(smem_raw);
   LmSmem& s = *reinterpret_cast<LmSmem*>(ring + kLmStages * kLmStageBytes);
@@ -95,6 +99,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (gate) tma_prefetch_desc(&tmH);
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem, kLmTmemCols);
@@ -124,7 +129,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           uint8_t* a_dst = ring + st * kLmStageBytes;
           mbar_arrive_expect_tx(&s.full[st], kLmStageBytes);
           tma_load_2d(a_dst, &tmA, kb * kBK, mt * 128, &s.full[st], pol_a);
-          tma_load_2d(a_dst + kLmABytes, &tmB, kb * kBK, (nt0 + i) * kLmBN, &s.full[st], pol_b);
+          if (nt0 + i == n_vocab_tiles)   // the gate tile (only when folded in)
+            tma_load_2d(a_dst + kLmABytes, &tmH, kb * kBK, 0, &s.full[st], pol_a);
+          else
+            tma_load_2d(a_dst + kLmABytes, &tmB, kb * kBK, (nt0 + i) * kLmBN, &s.full[st], pol_b);
           issued = it + 1;
         }
       }
@@ -182,6 +190,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tc_fence_after();
+      if (nt0 + i == n_vocab_tiles) {
+        // gate tile: H[row, c] = sigmoid(acc + b_H[c])
+#pragma unroll 1
+        for (int c = 0; c < kLmBN / 32; ++c) {
+          float v[32];
+          tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kLmBN + c * 32, v);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          float* dst = gate + static_cast<int64_t>(row) * kEmbed + c * 32;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o[u] = 1.0f / (1.0f + expf(-(v[j + u] + (b_H ? b_H[c * 32 + j + u] : 0.0f))));
+            *reinterpret_cast<float4*>(dst + j) = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[buf]);
+        continue;
+      }
       const int64_t id_base = static_cast<int64_t>(nt0 + i) * kLmBN;
 #pragma unroll 1
       for (int c = 0; c < kLmBN / 32; ++c) {
@@ -309,18 +340,28 @@ cudaError_t lmhead_noalloc_scratch(int device, void** ptr) {
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms) {
   (void)d;
-  const LmPlan p = lm_plan(M, V, num_sms);
-  return static_cast<size_t>(M) * p.n_runs * kTopK * sizeof(uint64_t);
+  // covers the plain head and the head with the gate tile folded in
+  const LmPlan p = lm_plan(M, V, num_sms), pg = lm_plan(M, V + kLmBN, num_sms);
+  const int n_runs = p.n_runs > pg.n_runs ? p.n_runs : pg.n_runs;
+  return static_cast<size_t>(M) * n_runs * kTopK * sizeof(uint64_t);
 }
 
-cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,
-                               int64_t d, float* vals, int32_t* idx, void* workspace, int num_sms,
-                               uint32_t* err, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_lmhead(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H, const float* b_H,
+                          int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx, float* gate, void* workspace,
+                          int num_sms, uint32_t* err, cudaStream_t stream) {
   if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const LmPlan p = lm_plan(M, V, num_sms);
-  CUtensorMap ta, tb;
+  const int n_vocab_tiles = static_cast<int>((V + kLmBN - 1) / kLmBN);
+  const LmPlan p = lm_plan(M, gate ? V + kLmBN : V, num_sms);
+  CUtensorMap ta, tb, th;
   if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, kLmBN))
     return cudaErrorInvalidValue;
+  if (gate) {
+    if (!make_tmap_bf16_2d(&th, W_H, kEmbed, d, d, kLmBN)) return cudaErrorInvalidValue;
+  } else {
+    th = tb;
+  }
   const size_t smem = 1024 + kLmStages * kLmStageBytes + sizeof(LmSmem);
   static bool configured = false;
   if (!configured) {
@@ -330,15 +371,30 @@ cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_
     configured = true;
   }
   uint64_t* partial = static_cast<uint64_t*>(workspace);
-  lmhead_kernel<<<p.grid, kLmThreads, smem, stream>>>(ta, tb, static_cast<int>(M), V, static_cast<int>(d),
-                                                       p.m_tiles, p.n_tiles, p.tiles_per_run, p.n_runs, partial,
-                                                       err);
+  lmhead_kernel<<<p.grid, kLmThreads, smem, stream>>>(ta, tb, th, static_cast<int>(M), V, static_cast<int>(d),
+                                                       p.m_tiles, p.n_tiles, n_vocab_tiles, p.tiles_per_run,
+                                                       p.n_runs, partial, gate, b_H, err);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows_per_block = 8;
   lmhead_merge_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,
                         stream>>>(partial, static_cast<int>(M), p.n_runs, vals, idx);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,
+                               int64_t d, float* vals, int32_t* idx, void* workspace, int num_sms,
+                               uint32_t* err, cudaStream_t stream) {
+  return launch_lmhead(hidden, W, nullptr, nullptr, M, V, d, vals, idx, nullptr, workspace, num_sms, err, stream);
+}
+
+cudaError_t launch_lmhead_topk_gate(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H,
+                                    const float* b_H, int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx,
+                                    float* gate, void* workspace, int num_sms, uint32_t* err,
+                                    cudaStream_t stream) {
+  return launch_lmhead(hidden, W, W_H, b_H, M, V, d, vals, idx, gate, workspace, num_sms, err, stream);
 }
 
 }  // namespace dflash2

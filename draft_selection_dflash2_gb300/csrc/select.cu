@@ -9,12 +9,11 @@
 // pair_kernel      one CTA per block position (b, t): gathers the 16 predecessor
 //                  rows of A and the 16 candidate rows of B (512 B each) with
 //                  16-byte loads, forms G = A_pred (.) H_t in fp32 shared memory,
-//                  and computes the 16 x 16 x 256 products with a 4 x 4 register
-//                  tile per thread over 16 interleaved slices of r, reduced by a
-//                  15-shuffle reduce-scatter.
+//                  and computes the 16 x 16 x 256 products (pair_math.cuh).
 #include "common.cuh"
 #include "gemm_splitk.cuh"
 #include "launch.h"
+#include "pair_math.cuh"
 
 namespace dflash2 {
 namespace {
@@ -116,46 +115,7 @@ __global__ void __launch_bounds__(256) pair_kernel(const int32_t* __restrict__ c
     }
   }
   __syncthreads();
-  // thread = (block of 4 x 4 outputs, slice rs of r).  Slice rs owns the float4
-  // chunks rs, rs + 16, rs + 32, rs + 48 of every row (conflict-free LDS.128).
-  const int rs = tid & 15, blk = tid >> 4;
-  const int ib = blk >> 2, jb = blk & 3;
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int c = rs + 16 * m;
-    float4 g[4], bb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) g[i] = *reinterpret_cast<const float4*>(&G[4 * ib + i][4 * c]);
-#pragma unroll
-    for (int jx = 0; jx < 4; ++jx) bb[jx] = *reinterpret_cast<const float4*>(&Bc[4 * jb + jx][4 * c]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int jx = 0; jx < 4; ++jx) {
-        float a = acc[i * 4 + jx];
-        a = fmaf(g[i].x, bb[jx].x, a);
-        a = fmaf(g[i].y, bb[jx].y, a);
-        a = fmaf(g[i].z, bb[jx].z, a);
-        a = fmaf(g[i].w, bb[jx].w, a);
-        acc[i * 4 + jx] = a;
-      }
-  }
-  // reduce-scatter over the 16 slices (lane bits 0..3): lane rs ends with output rs
-#pragma unroll
-  for (int half = 8; half >= 1; half >>= 1) {
-    const bool upper = (rs & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? acc[i] : acc[i + half];
-      const float keep = upper ? acc[i + half] : acc[i];
-      acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, half);
-    }
-  }
-  const int i = 4 * ib + (rs >> 2), j = 4 * jb + (rs & 3);
-  S[(pos * kTopK + i) * kTopK + j] = cand_val[pos * kTopK + j] + acc[0];
+  pair_products(G, Bc, cand_val, S, pos, tid);
 }
 
 }  // namespace

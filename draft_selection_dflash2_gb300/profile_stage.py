@@ -6,9 +6,11 @@ times, so that a profiler (ncu) can capture that stage's kernels alone.
 
 Stages: topk, pairs (gate + pair scores), walk0, walk1, conv (one application),
 verify0, verify1, lmhead (M=1024 hidden rows against the full vocabulary),
-viterbi (the exact best-path walk on N(0, 4) scores of B sequences) and eval
-(the Table 1 selector evaluation of B sequences of 7 positions with uniform
-candidate ids and the true token in slot 0 of 80% of the rows).
+lmhead_gate (the same with the context gate folded in), viterbi (the exact
+best-path walk on N(0, 4) scores of B sequences), eval (the Table 1 selector
+evaluation of B sequences of 7 positions with uniform candidate ids and the
+true token in slot 0 of 80% of the rows) and proj (projection-form pair scores
+of B sequences: A, B projected from an N(0, 1) [V, d] embedding).
 """
 import argparse
 import os
@@ -33,7 +35,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--stage", required=True,
                     choices=["topk", "pairs", "walk0", "walk1", "conv", "verify0", "verify1", "lmhead",
-                             "viterbi", "eval"])
+                             "lmhead_gate", "viterbi", "eval", "proj"])
     ap.add_argument("--B", type=int, default=128)
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
@@ -91,12 +93,27 @@ def main():
         hit = torch.rand((B, Le), generator=g, device="cuda") < 0.8
         cand[:, :, 0] = torch.where(hit, gt, cand[:, :, 0])
         run = lambda: api.selector_eval(h, gt, cand)  # noqa: E731
+    elif args.stage == "proj":
+        g = torch.Generator(device="cuda")
+        g.manual_seed(7)
+        ci = torch.randint(0, V, (B, L, K), generator=g, device="cuda", dtype=torch.int32)
+        cv = torch.randn((B, L, K), generator=g, device="cuda")
+        lv = torch.randint(0, V, (B,), generator=g, device="cuda", dtype=torch.int32)
+        H = torch.rand((B, L, R), generator=g, device="cuda")
+        E = torch.randn((V, D), generator=g, device="cuda").to(torch.bfloat16)
+        WA = (torch.randn((R, D), generator=g, device="cuda") / D ** 0.5).to(torch.bfloat16)
+        WB = (torch.randn((R, D), generator=g, device="cuda") / D ** 0.5).to(torch.bfloat16)
+        run = lambda: api.pair_scores_proj(h, ci, cv, lv, H, E, WA, WB)  # noqa: E731
     else:
         M = 1024
         hidden = bf(torch, synth.normal_bits(1, (M, D)))
         W = bf(torch, synth.normal_bits(2, (V, D), std=0.02))
         ws = torch.empty(max(api.lmhead_topk_workspace(h, M, V, D), 256), dtype=torch.uint8, device="cuda")
-        run = lambda: api.lmhead_topk(h, hidden, W, workspace=ws)  # noqa: E731
+        if args.stage == "lmhead_gate":
+            W_H = bf(torch, synth.normal_bits(3, (R, D), std=0.02))
+            run = lambda: api.lmhead_topk_gate(h, hidden, W, W_H, workspace=ws)  # noqa: E731
+        else:
+            run = lambda: api.lmhead_topk(h, hidden, W, workspace=ws)  # noqa: E731
     for _ in range(args.reps):
         run()
     torch.cuda.synchronize()

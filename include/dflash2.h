@@ -6,12 +6,14 @@
  * Inco AI):
  *   dflash2_topk          top-16 candidates per block position
  *   dflash2_pair_scores   context gate + pairwise path-selector scores
+ *   dflash2_pair_scores_proj  the same scores with A, B projected from E
  *   dflash2_walk          greedy or temperature-sampled walk over the scores
  *   dflash2_walk_viterbi  exact best path over the same scores
  *   dflash2_selector_eval Table 1's recall and acceptance-length evaluation
  *   dflash2_conv2tap      two-tap dynamic depthwise convolution
  *   dflash2_verify        block verification -> acceptance lengths
  *   dflash2_lmhead_topk   LM head GEMM with a streaming top-16 epilogue
+ *   dflash2_lmhead_topk_gate  the same with the context gate folded in
  *
  * Conventions for every call
  *   - Pointers marked "device" are CUDA device pointers on the handle's device;
@@ -126,6 +128,37 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
                         const int32_t* last_verified, const uint16_t* hs, const uint16_t* W_H,
                         const float* b_H, const uint16_t* A, const uint16_t* Bt, int64_t B,
                         int64_t L, int64_t d, int64_t V, float* gate, float* S, void* stream);
+
+/*
+ * Pair scores in projection form.  The score equation of "A Lightweight Path
+ * Selector" matches 256-dimensional embeddings of the predecessor and the
+ * candidate; here they are projections of the shared token embedding E,
+ *   A(a) = W_A E(a),   B(b) = W_B E(b),
+ * computed on the tensor cores (fp32 accumulation, not rounded) for exactly
+ * the tokens of the step, then
+ *   S[b,t,i,j] = cand_val[b,t,j] + sum_r A(pred_i)_r H[b,t,r] B(cand_j)_r
+ * with the predecessors of dflash2_pair_scores.
+ *   cand_idx, cand_val  device [B, L, 16] int32 / fp32
+ *   last_verified       device int32 [B]
+ *   gate                device fp32 [B, L, 256]: H, 16-byte aligned (e.g. the gate
+ *                       output of dflash2_lmhead_topk_gate or dflash2_pair_scores)
+ *   E                   device bf16 [V, d] shared token embedding
+ *   W_A, W_B            device bf16 [256, d]
+ *   P, P_bytes          device fp32 workspace of at least
+ *                       dflash2_pair_scores_proj_workspace(h, B, L) bytes, 16-byte
+ *                       aligned; on return it holds the projections, row
+ *                       (b*L + t)*16 + j for candidate j of (b, t), then row
+ *                       B*L*16 + b for last_verified[b]; each row is A (256) then B (256)
+ *   S                   device fp32 [B, L, 16, 16] output
+ * d % 64 == 0, L <= 64, B * L < 2^26.  Ids outside [0, V) are clamped and
+ * flagged (DFLASH2_DEVERR_BAD_TOKEN).  A bounded wait that gives up raises
+ * DFLASH2_DEVERR_TIMEOUT.
+ */
+size_t dflash2_pair_scores_proj_workspace(const dflash2_handle* h, int64_t B, int64_t L);
+int dflash2_pair_scores_proj(dflash2_handle* h, const int32_t* cand_idx, const float* cand_val,
+                             const int32_t* last_verified, const float* gate, const uint16_t* E,
+                             const uint16_t* W_A, const uint16_t* W_B, int64_t B, int64_t L, int64_t d, int64_t V,
+                             float* P, size_t P_bytes, float* S, void* stream);
 
 /*
  * The walk over precomputed scores.  "A Lightweight Path Selector": from the
@@ -251,6 +284,20 @@ size_t dflash2_lmhead_topk_workspace(const dflash2_handle* h, int64_t M, int64_t
 int dflash2_lmhead_topk(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
                         int64_t V, int64_t d, float* vals, int32_t* idx, void* workspace,
                         size_t ws_bytes, void* stream);
+
+/*
+ * Fused LM head + top-16 with the context gate folded in: W_H's 256 rows are
+ * one more 256-row tile of the same GEMM (0.17% more products at V = 151936),
+ * whose epilogue writes H = sigmoid(hidden W_H^T + b_H) instead of ranking.
+ * vals and idx are those of dflash2_lmhead_topk on the same inputs.
+ *   W_H   device bf16 [256, d];  b_H device fp32 [256] or NULL (= 0)
+ *   gate  device fp32 [M, 256], 16-byte aligned
+ * Other arguments, the workspace (dflash2_lmhead_topk_workspace covers both
+ * forms) and the limits are those of dflash2_lmhead_topk.
+ */
+int dflash2_lmhead_topk_gate(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H,
+                             const float* b_H, int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx,
+                             float* gate, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * dflash2_lmhead_topk without a workspace argument, for callers that cannot
