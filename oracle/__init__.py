@@ -43,6 +43,8 @@ def _load():
         lib.oracle_gate.restype = None
         lib.oracle_pair_scores.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, P, I]
         lib.oracle_pair_scores.restype = I
+        lib.oracle_gemm_conv2tap.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, I]
+        lib.oracle_gemm_conv2tap.restype = None
         lib.oracle_pair_scores_proj.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, P, I]
         lib.oracle_pair_scores_proj.restype = I
         lib.oracle_walk.argtypes = [P, P, I64, I64, I64, D, U64, U64, P, P, P, P, I]
@@ -218,6 +220,23 @@ def conv2tap(x_bits, x_prev_bits, k0_bits, k1_bits, W_c_bits, b_c=None, h_bits=N
     y = np.zeros((B, L, d), np.float64)
     _load().oracle_conv2tap(_p(x), _p(xp), _p(h), _p(k0), _p(k1), _p(W), _p(bc), B, L, d, _p(y),
                             nthreads or default_threads())
+    return y
+
+
+def gemm_conv2tap(A_bits, W_bits, x_prev_bits, h_bits, k0_bits, k1_bits, W_c_bits, b_c=None, nthreads=None):
+    """Conv fused into the producing GEMM (reading R20): A: uint16 [B, L, K]; W: uint16 [d, K];
+    x_prev: uint16 [B, d]; h: uint16 [B, L, d] -> y f64 [B, L, d] with x = A W^T exact."""
+    A = _c(A_bits, np.uint16)
+    W = _c(W_bits, np.uint16)
+    xp = _c(x_prev_bits, np.uint16)
+    hh = _c(h_bits, np.uint16)
+    k0, k1, Wc = _c(k0_bits, np.uint16), _c(k1_bits, np.uint16), _c(W_c_bits, np.uint16)
+    bc = _c(b_c, np.float32)
+    B, L, K = A.shape
+    d = W.shape[0]
+    y = np.zeros((B, L, d), np.float64)
+    _load().oracle_gemm_conv2tap(_p(A), _p(W), _p(xp), _p(hh), _p(k0), _p(k1), _p(Wc), _p(bc), B, L, K, d, _p(y),
+                                 nthreads or default_threads())
     return y
 
 

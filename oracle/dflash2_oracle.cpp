@@ -48,6 +48,10 @@
 //       parameter count, 3 x 256 x d for W_A, W_B and W_H, matches the 2.0M
 //       the pages state at d = 2560).  The projections are exact sums, not
 //       rounded to bf16 (the tables of R10 are this form folded offline).
+//   R20 conv fused into the producing GEMM: x = A W^T (the sublayer's output
+//       projection) is exact, with no rounding to bf16 between the GEMM and the
+//       taps, and the correction reads a given hidden state h (a GEMM epilogue
+//       sees one tile of x, never the whole row that W_c x would need).
 //   R18 selector evaluation (Table 1): recall at position t counts sequences
 //       whose earlier positions were all correct under the same rule (top-1
 //       equal to the true token, or the true token among the 16); the
@@ -419,6 +423,45 @@ void oracle_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* 
       const int64_t g = ch / 16;
       y[m * d + ch] = (widen_bf16(k0[ch]) + c[g]) * widen_bf16(x[m * d + ch]) +
                       (widen_bf16(k1[ch]) + c[G + g]) * widen_bf16(xp[ch]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 4, fused into the producing GEMM (reading R20): the conv's input is the
+// output of the sublayer's projection, x = A W^T, taken exactly:
+//   x[m, ch] = sum_k A[m, k] W[ch, k]
+//   c[m, n]  = sum_k W_c[n, k] h[m, k] (+ b_c[n])
+//   y[m, ch] = (k0[ch] + c[m, g]) x[m, ch] + (k1[ch] + c[m, G + g]) xp[ch]
+// with xp = x[m - 1] for t > 0 and x_prev[b] (bf16) at t = 0.
+// A: [B, L, K] bf16; W: [d, K] bf16; h: [B, L, d] bf16; the rest as
+// oracle_conv2tap; y: [B, L, d] double.
+// ---------------------------------------------------------------------------
+void oracle_gemm_conv2tap(const uint16_t* A, const uint16_t* W, const uint16_t* x_prev, const uint16_t* h,
+                          const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c, const float* b_c, int64_t B,
+                          int64_t L, int64_t K, int64_t d, double* y, int nthreads) {
+  const int64_t G = d / 16;
+#pragma omp parallel for schedule(static) num_threads(threads_for(nthreads))
+  for (int64_t b = 0; b < B; ++b) {
+    std::vector<double> x(static_cast<size_t>(L * d)), c(static_cast<size_t>(2 * G));
+    for (int64_t t = 0; t < L; ++t)
+      for (int64_t ch = 0; ch < d; ++ch) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) acc += widen_bf16(A[((b * L + t) * K) + k]) * widen_bf16(W[ch * K + k]);
+        x[t * d + ch] = acc;
+      }
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t m = b * L + t;
+      for (int64_t n = 0; n < 2 * G; ++n) {
+        double acc = b_c ? static_cast<double>(b_c[n]) : 0.0;
+        for (int64_t k = 0; k < d; ++k) acc += widen_bf16(W_c[n * d + k]) * widen_bf16(h[m * d + k]);
+        c[n] = acc;
+      }
+      for (int64_t ch = 0; ch < d; ++ch) {
+        const int64_t g = ch / 16;
+        const double xp = (t > 0) ? x[(t - 1) * d + ch] : widen_bf16(x_prev[b * d + ch]);
+        y[m * d + ch] = (widen_bf16(k0[ch]) + c[g]) * x[t * d + ch] + (widen_bf16(k1[ch]) + c[G + g]) * xp;
+      }
     }
   }
 }

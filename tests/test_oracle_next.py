@@ -235,3 +235,46 @@ def test_projection_with_integer_embeddings_matches_exact_tables():
     # a zero W_B removes the pair term: the scores are the candidate logits
     S0, _ = oracle.pair_scores_proj(ci, cv, lv, H, bits(Ei), bits(WAi), bits(0 * WBi))
     assert np.array_equal(S0, np.broadcast_to(cv[:, :, None, :], S0.shape).astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# conv fused into the producing GEMM (reading R20), pinned to the conv
+# (already pinned) through GEMMs whose output is exact in bf16
+# ---------------------------------------------------------------------------
+def _conv_parts(seed, B, L, d, bias):
+    from draft_selection_dflash2_gb300 import synth
+    c = synth.conv_inputs(seed, B, L, d, with_bias=bias)
+    h = synth.normal_bits(seed + 50, (B, L, d))
+    return synth, c, h
+
+
+def test_fused_conv_with_identity_projection_is_the_conv():
+    # W = I (K = d) and A = x: the GEMM returns x exactly
+    B, L, d = 2, 5, 64
+    synth, c, h = _conv_parts(1, B, L, d, True)
+    I = np.zeros((d, d), np.uint16)
+    I[np.arange(d), np.arange(d)] = synth.bf16_bits(np.float32(1.0))
+    y = oracle.gemm_conv2tap(c.x, I, c.x_prev, h, c.k0, c.k1, c.W_c, b_c=c.b_c)
+    ref = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c, b_c=c.b_c, h_bits=h)
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-14)
+
+
+def test_fused_conv_with_integer_projection_matches_conv_of_exact_x():
+    # A, W in {-1, 0, 1} with K = 96: A W^T is an exact integer (numpy integer matmul),
+    # exact in bf16, so the conv of its bf16 image is the fused result
+    B, L, d, K = 3, 4, 128, 96
+    synth, c, h = _conv_parts(2, B, L, d, False)
+    rng = np.random.default_rng(9)
+    Ai, Wi = rng.integers(-1, 2, (B, L, K)), rng.integers(-1, 2, (d, K))
+    bits = lambda a: synth.bf16_bits(a.astype(np.float32))          # noqa: E731
+    y = oracle.gemm_conv2tap(bits(Ai), bits(Wi), c.x_prev, h, c.k0, c.k1, c.W_c)
+    ref = oracle.conv2tap(bits(Ai @ Wi.T), c.x_prev, c.k0, c.k1, c.W_c, h_bits=h)
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-13)
+    # k0 = 0, k1 = 1, no correction: y is x shifted by one position, the first
+    # position of each block reading x_prev
+    zero = np.zeros_like(c.k0)
+    one = np.full_like(c.k1, synth.bf16_bits(np.float32(1.0)))
+    y1 = oracle.gemm_conv2tap(bits(Ai), bits(Wi), c.x_prev, h, zero, one, 0 * c.W_c)
+    x = (Ai @ Wi.T).astype(np.float64)
+    assert np.array_equal(y1[:, 1:], x[:, :-1])
+    assert np.array_equal(y1[:, 0], synth.bf16_to_f32(c.x_prev).astype(np.float64))
