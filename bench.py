@@ -99,12 +99,14 @@ _SOURCES = {
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
     "viterbi": ["viterbi.cu", "common.cuh"],
     "eval": ["eval.cu", "common.cuh"],
+    "gemm_conv": ["gemm_conv.cu", "tcgen05.cuh", "common.cuh"],
 }
 _PROFILE_SOURCES = {"conv2tap_B128_d5120.md": "conv2tap", "topk16_B128_V151936.md": "topk16",
                     "gate_gemm_B128_d5120.md": "pair_scores", "pair_kernel_B128.md": "pair_scores",
                     "verify_kernel_T0_B128.md": "verify", "verify_kernel_T1_B128.md": "verify",
                     "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead",
-                    "walk_viterbi_B16384.md": "viterbi", "selector_eval_B524288.md": "eval"}
+                    "walk_viterbi_B16384.md": "viterbi", "selector_eval_B524288.md": "eval",
+                    "proj_kernel_B128_d5120.md": "proj", "gemm_conv_kernel_B128_K5120_d5120.md": "gemm_conv"}
 
 
 def _source_hash(kernel):
@@ -594,8 +596,38 @@ def run_next(torch, api, h, cyc, dev, pk, B_vit=65536, B_eval=1 << 21):
         "ms": round(ms_p, 4), "table_form_pairs_ms_in_step": None,
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tf / pk["bf16_tflops"], 4),
-                     "note": "whole call (projection GEMM + pair kernel) against the projection's flops"}}
+                     "note": "whole call (projection GEMM + pair kernel) against the projection's flops",
+                     "traffic": profiled_traffic(["proj_kernel_B128_d5120.md"])}}
     del P, Sp, WA, WB
+
+    # the conv fused into its producing GEMM (an output projection K = d) against the
+    # library GEMM (cuBLAS, bf16 x) followed by the conv kernel; L2 flushed before each call
+    Kp = D
+    A = torch.randn((nb, L, Kp), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    Wp = (torch.randn((D, Kp), generator=g, device=dev, dtype=torch.float32) / Kp ** 0.5).to(torch.bfloat16)
+    hs = torch.randn((nb, L, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    x_prev, k0, k1, W_c = cyc.conv[0][1], cyc.conv[0][2], cyc.conv[0][3], cyc.conv[0][4]
+    c_work = torch.empty(((api.gemm_conv2tap_workspace(h, nb, L, D) + 3) // 4,), dtype=torch.float32, device=dev)
+    y = torch.empty((nb, L, D), dtype=torch.bfloat16, device=dev)
+    x = torch.empty((nb * L, D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ms_f = _timed(torch, lambda: flush.zero_(), reps=9)
+    fused = _timed(torch, lambda: (flush.zero_(), api.gemm_conv2tap(h, A, Wp, x_prev, hs, k0, k1, W_c, c_work=c_work,
+                                                                    y=y)), reps=9) - ms_f
+    unfused = _timed(torch, lambda: (flush.zero_(), torch.matmul(A.view(nb * L, Kp), Wp.t(), out=x),
+                                     api.conv2tap(h, x.view(nb, L, D), x_prev, k0, k1, W_c, hs=hs, y=y)),
+                     reps=9) - ms_f
+    del flush
+    flops = 2.0 * nb * L * D * (Kp + 2 * (D // 16))
+    tf = flops / (fused * 1e-3) / 1e12
+    out["conv_fused_gemm"] = {
+        "workload": f"B={nb} L={L} K={Kp} d={D}: y = conv(A W^T), correction from a given hidden state",
+        "fused_ms": round(fused, 4), "unfused_cublas_plus_conv_ms": round(unfused, 4),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / pk["bf16_tflops"], 4),
+                     "note": "whole call (one persistent kernel: correction and fused tiles) against both GEMMs' flops",
+                     "traffic": profiled_traffic(["gemm_conv_kernel_B128_K5120_d5120.md"])}}
+    del A, Wp, hs, c_work, y, x
 
     r1, r16 = table1_recalls()
     Le = len(r1)

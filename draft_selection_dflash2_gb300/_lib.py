@@ -38,6 +38,8 @@ SIGNATURES = {
     "dflash2_lmhead_topk": (I32, [P, P, P, I64, I64, I64, P, P, P, SZ, P]),
     "dflash2_lmhead_topk_gate": (I32, [P, P, P, P, P, I64, I64, I64, P, P, P, P, SZ, P]),
     "dflash2_pair_scores_proj_workspace": (SZ, [P, I64, I64]),
+    "dflash2_gemm_conv2tap_workspace": (SZ, [P, I64, I64, I64]),
+    "dflash2_gemm_conv2tap": (I32, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, SZ, P, I32, P]),
     "dflash2_pair_scores_proj": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, SZ, P, P]),
     "dflash2_lmhead_topk_noalloc": (I32, [P, P, P, I64, I64, I64, P, P, P]),
 }

@@ -188,6 +188,34 @@ def conv2tap(h: Handle, x, x_prev, k0, k1, W_c, b_c=None, hs=None, y=None, y_fp3
     return y
 
 
+def gemm_conv2tap_workspace(h: Handle, B: int, L: int, d: int) -> int:
+    return h._lib.dflash2_gemm_conv2tap_workspace(h.ptr, B, L, d)
+
+
+def gemm_conv2tap(h: Handle, A, W, x_prev, hs, k0, k1, W_c, b_c=None, c_work=None, y=None, y_fp32: bool = False,
+                  stream=None):
+    """Conv fused into its producing GEMM: A [B, L, K] bf16, W [d, K] bf16 -> (y [B, L, d], c fp32 [B*L, 2d/16]).
+
+    c_work: workspace of at least gemm_conv2tap_workspace(h, B, L, d) bytes (the correction, then
+    per-row-tile counters); allocated when None."""
+    B, L, Kd = A.shape
+    d = W.shape[0]
+    dev = A.device
+    for name, t in (("A", A), ("W", W), ("x_prev", x_prev), ("hs", hs), ("W_c", W_c)):
+        _need(_is16(t) and t.is_contiguous(), f"{name}: contiguous bf16")
+    if c_work is None:
+        c_work = torch.empty(((gemm_conv2tap_workspace(h, B, L, d) + 3) // 4,), dtype=torch.float32, device=dev)
+    if y is None:
+        y = torch.empty((B, L, d), dtype=torch.float32 if y_fp32 else torch.bfloat16, device=dev)
+    y_is_fp32 = 1 if y.dtype == torch.float32 else 0
+    _check(h._lib.dflash2_gemm_conv2tap(h.ptr, _ptr(A), _ptr(W), _ptr(x_prev), _ptr(hs), _ptr(k0), _ptr(k1),
+                                        _ptr(W_c), _ptr(b_c), B, L, Kd, d, _ptr(c_work),
+                                        c_work.numel() * c_work.element_size(), _ptr(y), y_is_fp32, _stream(stream)),
+           "dflash2_gemm_conv2tap")
+    n = 2 * (d // 16)
+    return y, c_work.view(-1)[: B * L * n].view(B * L, n)
+
+
 def verify(h: Handle, target, draft_tok, draft_slot=None, draft_q=None, cand_idx=None,
            temperature: float = 0.0, seed: int = 0, offset: int = 0, V: int = None,
            accept_len=None, out_tok=None, stream=None):

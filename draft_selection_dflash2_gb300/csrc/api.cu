@@ -225,6 +225,27 @@ int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_pre
                                            h->err, h->num_sms, as_stream(stream)));
 }
 
+size_t dflash2_gemm_conv2tap_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d) {
+  if (bad_handle(h) || B <= 0 || L <= 0 || d <= 0) return 0;
+  return dflash2::gemm_conv_workspace_bytes(B, L, d);
+}
+
+int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* W, const uint16_t* x_prev,
+                          const uint16_t* hs, const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
+                          const float* b_c, int64_t B, int64_t L, int64_t K, int64_t d, float* c_work,
+                          size_t c_bytes, void* y, int y_is_fp32, void* stream) {
+  if (bad_handle(h) || B < 0 || L < 0 || K <= 0 || d <= 0) return DFLASH2_ERR_INVALID_ARG;
+  if (d % 64 != 0 || K % 64 != 0 || L > kMaxL || B * L >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
+  if (B == 0 || L == 0) return DFLASH2_OK;
+  if (!A || !W || !x_prev || !hs || !k0 || !k1 || !W_c || !c_work || !y) return DFLASH2_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(x_prev, 16) || !aligned(hs, 16) || !aligned(k0, 16) ||
+      !aligned(k1, 16) || !aligned(W_c, 16) || !aligned(c_work, 16) || !aligned(y, 16) || (b_c && !aligned(b_c, 4)))
+    return DFLASH2_ERR_MISALIGNED;
+  if (c_bytes < dflash2::gemm_conv_workspace_bytes(B, L, d)) return DFLASH2_ERR_WORKSPACE;
+  return launched(dflash2::launch_gemm_conv2tap(A, W, x_prev, hs, k0, k1, W_c, b_c, B, L, K, d, c_work, y, y_is_fp32,
+                                                h->err, h->num_sms, as_stream(stream)));
+}
+
 int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                    const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
                    int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,

@@ -51,6 +51,14 @@ cudaError_t launch_lmhead_topk_gate(const uint16_t* hidden, const uint16_t* W, c
                                     const float* b_H, int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx,
                                     float* gate, void* workspace, int num_sms, uint32_t* err, cudaStream_t stream);
 
+// The two-tap conv fused into its producing GEMM (gemm_conv.cu): c = W_c h +
+// b_c into c_work ([B*L, 2d/16] fp32), then y = taps(A W^T).
+size_t gemm_conv_workspace_bytes(int64_t B, int64_t L, int64_t d);
+cudaError_t launch_gemm_conv2tap(const uint16_t* A, const uint16_t* W, const uint16_t* x_prev, const uint16_t* hs,
+                                 const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c, const float* b_c,
+                                 int64_t B, int64_t L, int64_t K, int64_t d, float* c_work, void* y, int y_is_fp32,
+                                 uint32_t* err, int num_sms, cudaStream_t stream);
+
 // Projection-form pair scores: P = [W_A E(id); W_B E(id)] for the step's
 // candidates and last verified tokens, then S from P (proj.cu).
 size_t proj_rows(int64_t B, int64_t L);

@@ -9,8 +9,9 @@ verify0, verify1, lmhead (M=1024 hidden rows against the full vocabulary),
 lmhead_gate (the same with the context gate folded in), viterbi (the exact
 best-path walk on N(0, 4) scores of B sequences), eval (the Table 1 selector
 evaluation of B sequences of 7 positions with uniform candidate ids and the
-true token in slot 0 of 80% of the rows) and proj (projection-form pair scores
-of B sequences: A, B projected from an N(0, 1) [V, d] embedding).
+true token in slot 0 of 80% of the rows), proj (projection-form pair scores
+of B sequences: A, B projected from an N(0, 1) [V, d] embedding) and gemm_conv
+(the conv fused into an output projection with K = d).
 """
 import argparse
 import os
@@ -35,7 +36,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--stage", required=True,
                     choices=["topk", "pairs", "walk0", "walk1", "conv", "verify0", "verify1", "lmhead",
-                             "lmhead_gate", "viterbi", "eval", "proj"])
+                             "lmhead_gate", "viterbi", "eval", "proj", "gemm_conv"])
     ap.add_argument("--B", type=int, default=128)
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
@@ -93,6 +94,13 @@ def main():
         hit = torch.rand((B, Le), generator=g, device="cuda") < 0.8
         cand[:, :, 0] = torch.where(hit, gt, cand[:, :, 0])
         run = lambda: api.selector_eval(h, gt, cand)  # noqa: E731
+    elif args.stage == "gemm_conv":
+        A = bf(torch, synth.normal_bits(1, (B, L, D)))
+        Wp = bf(torch, synth.normal_bits(2, (D, D), std=D ** -0.5))
+        hs = bf(torch, synth.normal_bits(3, (B, L, D)))
+        xp = bf(torch, synth.normal_bits(4, (B, D)))
+        k0, k1, W_c = (bf(torch, a) for a in synth.conv_layer_params(5, D))
+        run = lambda: api.gemm_conv2tap(h, A, Wp, xp, hs, k0, k1, W_c)  # noqa: E731
     elif args.stage == "proj":
         g = torch.Generator(device="cuda")
         g.manual_seed(7)

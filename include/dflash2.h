@@ -11,6 +11,7 @@
  *   dflash2_walk_viterbi  exact best path over the same scores
  *   dflash2_selector_eval Table 1's recall and acceptance-length evaluation
  *   dflash2_conv2tap      two-tap dynamic depthwise convolution
+ *   dflash2_gemm_conv2tap the same conv fused into its producing GEMM
  *   dflash2_verify        block verification -> acceptance lengths
  *   dflash2_lmhead_topk   LM head GEMM with a streaming top-16 epilogue
  *   dflash2_lmhead_topk_gate  the same with the context gate folded in
@@ -236,6 +237,34 @@ int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_pre
                      const uint16_t* hs, const uint16_t* k0, const uint16_t* k1,
                      const uint16_t* W_c, const float* b_c, int64_t B, int64_t L, int64_t d,
                      void* y, int y_is_fp32, void* stream);
+
+/*
+ * The two-tap conv fused into the GEMM that produces its input (the output
+ * projection of a drafter sublayer; the conv sits before and after each
+ * attention and feed-forward sublayer, "A Lightweight Local Convolution"), so
+ * x never goes to memory:
+ *   x[b,t,:] = A[b,t,:] W^T            (tensor cores, fp32, not rounded to bf16)
+ *   [c0; c1][b,t,:] = W_c hs[b,t,:] (+ b_c)
+ *   y[b,t,ch] = (k0[ch] + c0[b,t,ch/16]) x[b,t,ch] + (k1[ch] + c1[b,t,ch/16]) xp[ch]
+ *   xp = x[b,t-1,:] for t > 0, x_prev[b,:] for t = 0.
+ * The correction reads the given hidden state hs (a GEMM epilogue sees one
+ * tile of x, never the whole row that W_c x would need).
+ *   A       device bf16 [B, L, K];  W device bf16 [d, K]
+ *   x_prev  device bf16 [B, d];  hs device bf16 [B, L, d]
+ *   k0, k1, W_c, b_c  as dflash2_conv2tap
+ *   c_work  device workspace of at least dflash2_gemm_conv2tap_workspace(h, B, L, d)
+ *           bytes, 16-byte aligned; on return it starts with [c0; c1] ([B*L, 2d/16] fp32),
+ *           followed by the kernel's per-row-tile counters
+ *   y       device [B, L, d], fp32 if y_is_fp32 else bf16 (round to nearest even),
+ *           16-byte aligned; must not overlap the inputs.
+ * d % 64 == 0, K % 64 == 0, L <= 64.  A bounded wait that gives up raises
+ * DFLASH2_DEVERR_TIMEOUT.
+ */
+size_t dflash2_gemm_conv2tap_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d);
+int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* W, const uint16_t* x_prev,
+                          const uint16_t* hs, const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
+                          const float* b_c, int64_t B, int64_t L, int64_t K, int64_t d, float* c_work,
+                          size_t c_bytes, void* y, int y_is_fp32, void* stream);
 
 /*
  * Block verification against the target's logits.  "A Lightweight Path
