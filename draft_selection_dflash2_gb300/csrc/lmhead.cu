@@ -7,8 +7,11 @@
 // lmhead_kernel (persistent, one CTA per SM):
 //   CTA c owns hidden-row tile mt = c % m_tiles (128 rows) and a contiguous run
 //   of vocabulary tiles (256 ids each), so the m_tiles CTAs sharing a run read
-//   the same W tiles at about the same time and W streams from HBM once (the
-//   other reads hit L2).
+//   the same W tiles at about the same time and W streams from HBM once.
+//   Consecutive CTAs (same run, different row tiles) form clusters of 2 that
+//   share each W tile: every member loads a slice of it with a TMA multicast
+//   into all members' rings, which halves the W reads from L2.  Each member's
+//   MMA commit frees a stage in every member.
 //   warp 0      TMA producer: 128 x 64 hidden tiles + 256 x 64 W tiles into a
 //               4-deep ring (48 KB per stage, 128-byte swizzle).
 //   warp 1      allocates 512 TMEM columns = two 128 x 256 fp32 accumulators;
@@ -43,6 +46,7 @@ constexpr int kLmBBytes = kLmBN * kTileRowBytes;               // 32 KB
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
 constexpr uint32_t kLmTmemCols = 2 * kLmBN;                    // double-buffered accumulator
 constexpr uint32_t kLmIdesc = umma_idesc_bf16(128, kLmBN);
+constexpr int kLmMaxCluster = 2;                                // CTAs sharing a W tile
 
 struct LmSmem {
   uint64_t full[kLmStages];
@@ -53,6 +57,32 @@ struct LmSmem {
   uint32_t tmem;
   int abort_flag;
 };
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The box at (x, y) of a 2-D tensor map into shared memory at the same offset
+// in every CTA of `mask` (this cluster), completing tx bytes on each one's `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask), "l"(policy)
+      : "memory");
+}
+
+// Arrives once on `bar` in every CTA of `mask` when this thread's tcgen05.mma so far are complete.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
 
 // Order-preserving 64-bit key of an fp32 logit and its id: larger key ranks
 // first (value descending, then id ascending); 0 is "empty".
@@ -72,7 +102,7 @@ __device__ __forceinline__ float logit_key_value(uint64_t k) {
 __global__ void __launch_bounds__(kLmThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmH, int M, int64_t V, int d, int m_tiles, int n_tiles,
-                  int n_vocab_tiles, int tiles_per_run, int n_runs, uint64_t* __restrict__ partial,
+                  int n_vocab_tiles, int tiles_per_run, int n_runs, int mc, uint64_t* __restrict__ partial,
                   float* __restrict__ gate, const float* __restrict__ b_H, uint32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = align_smem<1024>(smem_raw);
@@ -84,11 +114,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int nt1 = min(n_tiles, nt0 + tiles_per_run);
   const int ntiles = max(0, nt1 - nt0);
   const int nk = d / kBK;
+  // cluster of mc CTAs sharing each W tile: member `crank` loads rows
+  // [crank * wrows, +wrows) of it for all of them
+  const uint32_t crank = mc > 1 ? cluster_rank() : 0u;
+  const uint16_t cmask = static_cast<uint16_t>((1u << mc) - 1u);
+  const int wrows = kLmBN / mc;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLmStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
+      mbar_init(&s.empty[i], mc);        // one MMA commit from every member
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -108,6 +143,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (mc > 1) {
+    // every member's barriers exist before any multicast or remote arrival
+    cluster_arrive();
+    cluster_wait();
+  }
   const uint32_t tmem = s.tmem;
   volatile int* abort_flag = &s.abort_flag;
 
@@ -129,15 +169,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           uint8_t* a_dst = ring + st * kLmStageBytes;
           mbar_arrive_expect_tx(&s.full[st], kLmStageBytes);
           tma_load_2d(a_dst, &tmA, kb * kBK, mt * 128, &s.full[st], pol_a);
-          if (nt0 + i == n_vocab_tiles)   // the gate tile (only when folded in)
-            tma_load_2d(a_dst + kLmABytes, &tmH, kb * kBK, 0, &s.full[st], pol_a);
+          const bool gate_tile = nt0 + i == n_vocab_tiles;   // W_H (only when folded in)
+          const CUtensorMap* tw = gate_tile ? &tmH : &tmB;
+          const int wrow = (gate_tile ? 0 : (nt0 + i) * kLmBN) + static_cast<int>(crank) * wrows;
+          uint8_t* w_dst = a_dst + kLmABytes + static_cast<int>(crank) * wrows * kTileRowBytes;
+          if (mc > 1)
+            tma_load_2d_mc(w_dst, tw, kb * kBK, wrow, &s.full[st], cmask, gate_tile ? pol_a : pol_b);
           else
-            tma_load_2d(a_dst + kLmABytes, &tmB, kb * kBK, (nt0 + i) * kLmBN, &s.full[st], pol_b);
+            tma_load_2d(w_dst, tw, kb * kBK, wrow, &s.full[st], gate_tile ? pol_a : pol_b);
           issued = it + 1;
         }
       }
-      for (int j = issued - kLmStages > 0 ? issued - kLmStages : 0; j < issued; ++j)
+      for (int j = issued - kLmStages > 0 ? issued - kLmStages : 0; j < issued; ++j) {
         mbar_wait_bounded(&s.full[j % kLmStages], (j / kLmStages) & 1, err);
+        // every member's commit for the stage has arrived here before this CTA may exit
+        if (mc > 1) mbar_wait_bounded(&s.empty[j % kLmStages], (j / kLmStages) & 1, err);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -165,7 +212,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           for (int k = 0; k < kBK / 16; ++k)
             umma_bf16(acc, umma_desc_sw128(a_base + k * 32), umma_desc_sw128(b_base + k * 32), kLmIdesc,
                       (kb | k) != 0 ? 1u : 0u);
-          umma_commit(&s.empty[st]);
+          if (mc > 1)
+            umma_commit_mc(&s.empty[st], cmask);
+          else
+            umma_commit(&s.empty[st]);
         }
         umma_commit(&s.tfull[buf]);
         if (!ok) break;
@@ -270,6 +320,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kLmTmemCols);
   }
+  if (mc > 1) {
+    // no member leaves while another may still write into its shared memory
+    cluster_arrive();
+    cluster_wait();
+  }
 }
 
 // One warp per row: the top-16 of the row's n_runs partial lists.
@@ -353,28 +408,57 @@ cudaError_t launch_lmhead(const uint16_t* hidden, const uint16_t* W, const uint1
                           int num_sms, uint32_t* err, cudaStream_t stream) {
   if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const int n_vocab_tiles = static_cast<int>((V + kLmBN - 1) / kLmBN);
-  const LmPlan p = lm_plan(M, gate ? V + kLmBN : V, num_sms);
-  CUtensorMap ta, tb, th;
-  if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, kLmBN))
-    return cudaErrorInvalidValue;
-  if (gate) {
-    if (!make_tmap_bf16_2d(&th, W_H, kEmbed, d, d, kLmBN)) return cudaErrorInvalidValue;
-  } else {
-    th = tb;
-  }
+  const int64_t Vt = gate ? V + kLmBN : V;
   const size_t smem = 1024 + kLmStages * kLmStageBytes + sizeof(LmSmem);
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  // clusters of consecutive CTAs (same run, different row tiles) share W tiles;
+  // the runs are sized to the clusters that can be resident at once
+  const int m_tiles = static_cast<int>((M + 127) / 128);
+  int mc = 1;
+  while (mc < kLmMaxCluster && m_tiles % (2 * mc) == 0) mc *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kLmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(mc);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int slots = num_sms;
+  if (mc > 1) {
+    static int resident[kLmMaxCluster + 1] = {};
+    if (resident[mc] == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(mc), 1, 1);
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, lmhead_kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      resident[mc] = n > 0 ? n : 1;
+    }
+    slots = resident[mc] * mc;
+  }
+  const LmPlan p = lm_plan(M, Vt, slots);
+  CUtensorMap ta, tb, th;
+  if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, kLmBN / mc))
+    return cudaErrorInvalidValue;
+  if (gate) {
+    if (!make_tmap_bf16_2d(&th, W_H, kEmbed, d, d, kLmBN / mc)) return cudaErrorInvalidValue;
+  } else {
+    th = tb;
+  }
   uint64_t* partial = static_cast<uint64_t*>(workspace);
-  lmhead_kernel<<<p.grid, kLmThreads, smem, stream>>>(ta, tb, th, static_cast<int>(M), V, static_cast<int>(d),
-                                                       p.m_tiles, p.n_tiles, n_vocab_tiles, p.tiles_per_run,
-                                                       p.n_runs, partial, gate, b_H, err);
-  const cudaError_t e = cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lmhead_kernel, ta, tb, th, static_cast<int>(M), V, static_cast<int>(d),
+                                     p.m_tiles, p.n_tiles, n_vocab_tiles, p.tiles_per_run, p.n_runs, mc, partial,
+                                     gate, b_H, err);
   if (e != cudaSuccess) return e;
   const int rows_per_block = 8;
   lmhead_merge_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,

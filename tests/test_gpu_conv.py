@@ -58,3 +58,15 @@ def test_conv_identity_on_gpu(handle):
     c.W_c[:] = 0
     y = run(handle, c, y_fp32=False)
     assert np.array_equal(y, c.x)
+
+
+def test_conv_unsplit_large_batch_sampled(handle):
+    # B=512, L=16, d=5120: 64 row tiles x 2 column tiles fill the GPU without a K
+    # split, so each CTA reduces nothing and streams its own 128 rows; sequences
+    # checked against the oracle one by one (each depends only on its own rows)
+    B, L, d = 512, 16, 5120
+    c = synth.conv_inputs(41, B, L, d, with_bias=True)
+    y = run(handle, c)
+    for b in (0, 255, 511):
+        oy = oracle.conv2tap(c.x[b:b + 1], c.x_prev[b:b + 1], c.k0, c.k1, c.W_c, b_c=c.b_c)
+        assert_close(y[b:b + 1], oy, what=f"y (sequence {b})")
