@@ -8,20 +8,26 @@
 //   CTA c owns hidden-row tile mt = c % m_tiles (128 rows) and a contiguous run
 //   of vocabulary tiles (256 ids each), so the m_tiles CTAs sharing a run read
 //   the same W tiles at about the same time and W streams from HBM once.
-//   Consecutive CTAs (same run, different row tiles) form clusters of 2 that
-//   share each W tile: every member loads a slice of it with a TMA multicast
-//   into all members' rings, which halves the W reads from L2.  Each member's
-//   MMA commit frees a stage in every member.
-//   warp 0      TMA producer: 128 x 64 hidden tiles + 256 x 64 W tiles into a
-//               4-deep ring (48 KB per stage, 128-byte swizzle).
+//   Pair form (an even number of row tiles): consecutive CTAs (same run, row
+//   tiles 2j and 2j + 1) form a CTA pair that computes 256 x 256 tiles with
+//   tcgen05.mma.cta_group::2: each CTA holds its own 128 hidden rows and half of
+//   the W tile, so a 64-wide K stage brings 32 KB into each SM instead of 48 KB
+//   (what each SM can take in per clock sets the pace of these GEMMs).
+//   warp 0      TMA producer: 128 x 64 hidden tiles + the W tile (or, in the
+//               pair form, its 128-row half) into a 4-deep (pair form: 6-deep)
+//               ring with the 128-byte swizzle.  In the pair form both CTAs'
+//               loads complete on the leader's stage barrier.
 //   warp 1      allocates 512 TMEM columns = two 128 x 256 fp32 accumulators;
-//               lane 0 issues 4 tcgen05.mma (128 x 256 x 16) per stage into the
-//               current buffer and commits it when the tile's K loop is done.
+//               lane 0 issues 4 tcgen05.mma (128 x 256 x 16, or 256 x 256 x 16
+//               over the pair from the leader, rank 0) per stage into the
+//               current buffer and commits it when the tile's K loop is done;
+//               the pair form's commits arrive in both CTAs.
 //   warps 2..5  epilogue: each thread owns one hidden row (one TMEM lane) and
 //               keeps its running top-16 in registers; it reads the finished
 //               buffer 32 columns at a time (tcgen05.ld) and inserts the rare
-//               logits above its 16th best, then hands the buffer back, so
-//               the epilogue of tile i overlaps the MMAs of tile i + 1.
+//               logits above its 16th best, then hands the buffer back (to the
+//               leader, in the pair form), so the epilogue of tile i overlaps
+//               the MMAs of tile i + 1.
 //   At the end each thread writes its list as 16 order-preserving 64-bit keys
 //   (fp32 value, -id) to the workspace [M, n_runs, 16].
 //   With the context gate folded in, W_H's 256 rows are one more "vocabulary"
@@ -39,20 +45,25 @@ namespace dflash2 {
 namespace {
 
 constexpr int kLmBN = 256;
-constexpr int kLmStages = 4;
 constexpr int kLmThreads = 192;
 constexpr int kLmABytes = 128 * kTileRowBytes;                 // 16 KB
-constexpr int kLmBBytes = kLmBN * kTileRowBytes;               // 32 KB
-constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
+constexpr int kLmMaxStages = 6;
 constexpr uint32_t kLmTmemCols = 2 * kLmBN;                    // double-buffered accumulator
-constexpr uint32_t kLmIdesc = umma_idesc_bf16(128, kLmBN);
-constexpr int kLmMaxCluster = 2;                                // CTAs sharing a W tile
+
+// W rows per CTA, stage size and ring depth of each form
+template <bool kPair>
+struct LmForm {
+  static constexpr int kWRows = kPair ? kLmBN / 2 : kLmBN;
+  static constexpr int kStageBytes = kLmABytes + kWRows * kTileRowBytes;
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr uint32_t kIdesc = umma_idesc_bf16(kPair ? 256 : 128, kLmBN);
+};
 
 struct LmSmem {
-  uint64_t full[kLmStages];
-  uint64_t empty[kLmStages];
+  uint64_t full[kLmMaxStages];     // pair form: the leader's count both CTAs' bytes
+  uint64_t empty[kLmMaxStages];
   uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tempty[2];              // pair form: the leader's count both CTAs' epilogue warps
   uint64_t drain;
   uint32_t tmem;
   int abort_flag;
@@ -64,24 +75,74 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-// The box at (x, y) of a 2-D tensor map into shared memory at the same offset
-// in every CTA of `mask` (this cluster), completing tx bytes on each one's `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask, uint64_t policy) {
+// Address of this CTA's shared variable at `p` in the shared window of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+// Pair form: the box at (x, y) into this CTA's shared memory, completing tx
+// bytes on the barrier at cluster address `bar` (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask), "l"(policy)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 
-// Arrives once on `bar` in every CTA of `mask` when this thread's tcgen05.mma so far are complete.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+// Pair form: D[tmem] (+)= A B^T over both CTAs' operands at the same shared offsets.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(mask)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Pair form: arrives once on `bar` in both CTAs when the pair's MMAs so far are complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Pair form: arrives once on this CTA's `bar` when the pair's MMAs so far are complete.
+__device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Arrives once on the barrier at cluster address `bar` (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <bool kPair>
+__device__ __forceinline__ void lm_tmem_alloc(uint32_t* dst) {
+  if constexpr (kPair) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(kLmTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    tmem_alloc(dst, kLmTmemCols);
+    tmem_relinquish();
+  }
+}
+
+template <bool kPair>
+__device__ __forceinline__ void lm_tmem_dealloc(uint32_t taddr) {
+  if constexpr (kPair)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kLmTmemCols) : "memory");
+  else
+    tmem_dealloc(taddr, kLmTmemCols);
 }
 
 // Order-preserving 64-bit key of an fp32 logit and its id: larger key ranks
@@ -99,14 +160,17 @@ __device__ __forceinline__ float logit_key_value(uint64_t k) {
   return __uint_as_float(b);
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kLmThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmH, int M, int64_t V, int d, int m_tiles, int n_tiles,
-                  int n_vocab_tiles, int tiles_per_run, int n_runs, int mc, uint64_t* __restrict__ partial,
+                  int n_vocab_tiles, int tiles_per_run, int n_runs, uint64_t* __restrict__ partial,
                   float* __restrict__ gate, const float* __restrict__ b_H, uint32_t* __restrict__ err) {
+  using F = LmForm<kPair>;
+  constexpr int S = F::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = align_smem<1024>(smem_raw);
-  LmSmem& s = *reinterpret_cast<LmSmem*>(ring + kLmStages * kLmStageBytes);
+  LmSmem& s = *reinterpret_cast<LmSmem*>(ring + S * F::kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x % m_tiles;
   const int run = blockIdx.x / m_tiles;
@@ -114,20 +178,18 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int nt1 = min(n_tiles, nt0 + tiles_per_run);
   const int ntiles = max(0, nt1 - nt0);
   const int nk = d / kBK;
-  // cluster of mc CTAs sharing each W tile: member `crank` loads rows
-  // [crank * wrows, +wrows) of it for all of them
-  const uint32_t crank = mc > 1 ? cluster_rank() : 0u;
-  const uint16_t cmask = static_cast<uint16_t>((1u << mc) - 1u);
-  const int wrows = kLmBN / mc;
+  // pair form: rank 0 leads (issues the MMAs); rank r holds W rows [r * 128, +128) of each tile
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kLmStages; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], mc);        // one MMA commit from every member
+      mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);       // one arrival per epilogue warp
+      mbar_init(&s.tempty[i], kPair ? 8 : 4);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
@@ -136,18 +198,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     tma_prefetch_desc(&tmB);
     if (gate) tma_prefetch_desc(&tmH);
   }
-  if (warp == 1) {
-    tmem_alloc(&s.tmem, kLmTmemCols);
-    tmem_relinquish();
-  }
+  if (warp == 1) lm_tmem_alloc<kPair>(&s.tmem);
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (mc > 1) {
-    // every member's barriers exist before any multicast or remote arrival
+  if (kPair) {
+    // both CTAs' barriers and TMEM exist before any remote arrival or pair MMA
     cluster_arrive();
     cluster_wait();
   }
+  tc_fence_after();
   const uint32_t tmem = s.tmem;
   volatile int* abort_flag = &s.abort_flag;
 
@@ -160,34 +219,39 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol_b));
       int it = 0, issued = 0;
       for (int i = 0; i < ntiles && !*abort_flag; ++i) {
+        const bool gate_tile = nt0 + i == n_vocab_tiles;   // W_H (only when folded in)
+        const CUtensorMap* tw = gate_tile ? &tmH : &tmB;
+        const int wrow = (gate_tile ? 0 : (nt0 + i) * kLmBN) + static_cast<int>(rank) * F::kWRows;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % kLmStages;
-          if (it >= kLmStages && !mbar_wait_bounded(&s.empty[st], ((it / kLmStages) - 1) & 1, err)) {
+          const int st = it % S;
+          if (it >= S && !mbar_wait_bounded(&s.empty[st], ((it / S) - 1) & 1, err)) {
             *abort_flag = 1;
             break;
           }
-          uint8_t* a_dst = ring + st * kLmStageBytes;
-          mbar_arrive_expect_tx(&s.full[st], kLmStageBytes);
-          tma_load_2d(a_dst, &tmA, kb * kBK, mt * 128, &s.full[st], pol_a);
-          const bool gate_tile = nt0 + i == n_vocab_tiles;   // W_H (only when folded in)
-          const CUtensorMap* tw = gate_tile ? &tmH : &tmB;
-          const int wrow = (gate_tile ? 0 : (nt0 + i) * kLmBN) + static_cast<int>(crank) * wrows;
-          uint8_t* w_dst = a_dst + kLmABytes + static_cast<int>(crank) * wrows * kTileRowBytes;
-          if (mc > 1)
-            tma_load_2d_mc(w_dst, tw, kb * kBK, wrow, &s.full[st], cmask, gate_tile ? pol_a : pol_b);
-          else
-            tma_load_2d(w_dst, tw, kb * kBK, wrow, &s.full[st], gate_tile ? pol_a : pol_b);
+          uint8_t* a_dst = ring + st * F::kStageBytes;
+          if constexpr (kPair) {
+            // both CTAs' halves complete on the leader's barrier, which expects them all
+            if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * F::kStageBytes);
+            const uint32_t bar = cluster_addr(&s.full[st], 0);
+            tma_load_2d_pair(a_dst, &tmA, kb * kBK, mt * 128, bar, pol_a);
+            tma_load_2d_pair(a_dst + kLmABytes, tw, kb * kBK, wrow, bar, gate_tile ? pol_a : pol_b);
+          } else {
+            mbar_arrive_expect_tx(&s.full[st], F::kStageBytes);
+            tma_load_2d(a_dst, &tmA, kb * kBK, mt * 128, &s.full[st], pol_a);
+            tma_load_2d(a_dst + kLmABytes, tw, kb * kBK, wrow, &s.full[st], gate_tile ? pol_a : pol_b);
+          }
           issued = it + 1;
         }
       }
-      for (int j = issued - kLmStages > 0 ? issued - kLmStages : 0; j < issued; ++j) {
-        mbar_wait_bounded(&s.full[j % kLmStages], (j / kLmStages) & 1, err);
-        // every member's commit for the stage has arrived here before this CTA may exit
-        if (mc > 1) mbar_wait_bounded(&s.empty[j % kLmStages], (j / kLmStages) & 1, err);
+      // before this CTA may exit: its own copies have landed (the leader's
+      // barrier saw them) and the pair's MMAs are done with every stage
+      for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j) {
+        if (!kPair || leader) mbar_wait_bounded(&s.full[j % S], (j / S) & 1, err);
+        mbar_wait_bounded(&s.empty[j % S], (j / S) & 1, err);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int it = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int buf = i & 1;
@@ -199,25 +263,32 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const uint32_t acc = tmem + buf * kLmBN;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % kLmStages;
-          if (!mbar_wait_bounded(&s.full[st], (it / kLmStages) & 1, err) || *abort_flag) {
+          const int st = it % S;
+          if (!mbar_wait_bounded(&s.full[st], (it / S) & 1, err) || *abort_flag) {
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_addr(ring + st * kLmStageBytes);
+          const uint32_t a_base = smem_addr(ring + st * F::kStageBytes);
           const uint32_t b_base = a_base + kLmABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16(acc, umma_desc_sw128(a_base + k * 32), umma_desc_sw128(b_base + k * 32), kLmIdesc,
-                      (kb | k) != 0 ? 1u : 0u);
-          if (mc > 1)
-            umma_commit_mc(&s.empty[st], cmask);
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = umma_desc_sw128(a_base + k * 32), bd = umma_desc_sw128(b_base + k * 32);
+            if constexpr (kPair)
+              umma_bf16_pair(acc, ad, bd, F::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_bf16(acc, ad, bd, F::kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          if constexpr (kPair)
+            umma_commit_pair(&s.empty[st]);
           else
             umma_commit(&s.empty[st]);
         }
-        umma_commit(&s.tfull[buf]);
+        if constexpr (kPair)
+          umma_commit_pair(&s.tfull[buf]);
+        else
+          umma_commit(&s.tfull[buf]);
         if (!ok) break;
       }
     }
@@ -226,6 +297,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int q = warp & 3;
     const int row = mt * 128 + q * 32 + lane;
     const bool row_ok = row < M;
+    // the leader's MMA waits for every epilogue warp of the pair before reusing a buffer
+    const uint32_t tempty0 = kPair ? cluster_addr(&s.tempty[0], 0) : 0u;
+    const uint32_t tempty1 = kPair ? cluster_addr(&s.tempty[1], 0) : 0u;
     float val[kTopK];
     int32_t ids[kTopK];
 #pragma unroll
@@ -240,14 +314,27 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tc_fence_after();
-      if (nt0 + i == n_vocab_tiles) {
-        // gate tile: H[row, c] = sigmoid(acc + b_H[c])
+      const bool gate_tile = nt0 + i == n_vocab_tiles;
+      const int64_t id_base = static_cast<int64_t>(nt0 + i) * kLmBN;
 #pragma unroll 1
-        for (int c = 0; c < kLmBN / 32; ++c) {
-          float v[32];
-          tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kLmBN + c * 32, v);
-          tmem_ld_wait();
-          if (!row_ok) continue;
+      for (int c = 0; c < kLmBN / 32; ++c) {
+        float v[32];
+        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kLmBN + c * 32, v);
+        tmem_ld_wait();
+        if (c == kLmBN / 32 - 1) {
+          // the buffer is read out: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair)
+              mbar_arrive_cluster(buf ? tempty1 : tempty0);
+            else
+              mbar_arrive(&s.tempty[buf]);
+          }
+        }
+        if (!row_ok) continue;
+        if (gate_tile) {
+          // gate tile: H[row, c] = sigmoid(acc + b_H[c])
           float* dst = gate + static_cast<int64_t>(row) * kEmbed + c * 32;
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -257,20 +344,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               o[u] = 1.0f / (1.0f + expf(-(v[j + u] + (b_H ? b_H[c * 32 + j + u] : 0.0f))));
             *reinterpret_cast<float4*>(dst + j) = make_float4(o[0], o[1], o[2], o[3]);
           }
+          continue;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.tempty[buf]);
-        continue;
-      }
-      const int64_t id_base = static_cast<int64_t>(nt0 + i) * kLmBN;
-#pragma unroll 1
-      for (int c = 0; c < kLmBN / 32; ++c) {
-        float v[32];
-        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * kLmBN + c * 32, v);
-        tmem_ld_wait();
         const int64_t id0 = id_base + c * 32;
-        if (!row_ok) continue;
         // the common case (nothing above the row's 16th best) costs one compare
         // per logit; the sorted insertion stays a compact loop
         float m = v[0];
@@ -299,9 +375,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[buf]);
     }
     if (row_ok) {
       uint64_t* dst = partial + (static_cast<int64_t>(row) * n_runs + run) * kTopK;
@@ -311,19 +384,26 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && leader) {
     if (lane == 0) {
-      umma_commit(&s.drain);
+      if constexpr (kPair)
+        umma_commit_pair_local(&s.drain);
+      else
+        umma_commit(&s.drain);
       mbar_wait_bounded(&s.drain, 0, err);
     }
     __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kLmTmemCols);
   }
-  if (mc > 1) {
-    // no member leaves while another may still write into its shared memory
+  if (kPair) {
+    // the leader's MMAs are complete and every remote arrival has landed
+    // before either CTA frees its TMEM or leaves
+    tc_fence_before();
     cluster_arrive();
     cluster_wait();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    lm_tmem_dealloc<kPair>(tmem);
   }
 }
 
@@ -403,67 +483,75 @@ size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms) {
 
 namespace {
 
-cudaError_t launch_lmhead(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H, const float* b_H,
-                          int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx, float* gate, void* workspace,
-                          int num_sms, uint32_t* err, cudaStream_t stream) {
-  if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
+template <bool kPair>
+cudaError_t launch_lmhead_form(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H, const float* b_H,
+                               int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx, float* gate,
+                               void* workspace, int num_sms, uint32_t* err, cudaStream_t stream) {
+  using F = LmForm<kPair>;
   const int n_vocab_tiles = static_cast<int>((V + kLmBN - 1) / kLmBN);
   const int64_t Vt = gate ? V + kLmBN : V;
-  const size_t smem = 1024 + kLmStages * kLmStageBytes + sizeof(LmSmem);
+  const size_t smem = 1024 + F::kStages * F::kStageBytes + sizeof(LmSmem);
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  // clusters of consecutive CTAs (same run, different row tiles) share W tiles;
-  // the runs are sized to the clusters that can be resident at once
-  const int m_tiles = static_cast<int>((M + 127) / 128);
-  int mc = 1;
-  while (mc < kLmMaxCluster && m_tiles % (2 * mc) == 0) mc *= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kLmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(mc);
+  attr[0].val.clusterDim.x = kPair ? 2u : 1u;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int slots = num_sms;
-  if (mc > 1) {
-    static int resident[kLmMaxCluster + 1] = {};
-    if (resident[mc] == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(mc), 1, 1);
+  if (kPair) {
+    // the runs are sized to the pairs that can be resident at once
+    static int resident = 0;
+    if (resident == 0) {
+      cfg.gridDim = dim3(2, 1, 1);
       int n = 0;
-      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, lmhead_kernel, &cfg);
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, lmhead_kernel<kPair>, &cfg);
       if (e != cudaSuccess) return e;
-      resident[mc] = n > 0 ? n : 1;
+      resident = n > 0 ? n : 1;
     }
-    slots = resident[mc] * mc;
+    slots = 2 * resident;
   }
   const LmPlan p = lm_plan(M, Vt, slots);
   CUtensorMap ta, tb, th;
-  if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, kLmBN / mc))
+  if (!make_tmap_bf16_2d(&ta, hidden, M, d, d, 128) || !make_tmap_bf16_2d(&tb, W, V, d, d, F::kWRows))
     return cudaErrorInvalidValue;
   if (gate) {
-    if (!make_tmap_bf16_2d(&th, W_H, kEmbed, d, d, kLmBN / mc)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&th, W_H, kEmbed, d, d, F::kWRows)) return cudaErrorInvalidValue;
   } else {
     th = tb;
   }
   uint64_t* partial = static_cast<uint64_t*>(workspace);
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, lmhead_kernel, ta, tb, th, static_cast<int>(M), V, static_cast<int>(d),
-                                     p.m_tiles, p.n_tiles, n_vocab_tiles, p.tiles_per_run, p.n_runs, mc, partial,
-                                     gate, b_H, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, lmhead_kernel<kPair>, ta, tb, th, static_cast<int>(M), V,
+                                     static_cast<int>(d), p.m_tiles, p.n_tiles, n_vocab_tiles, p.tiles_per_run,
+                                     p.n_runs, partial, gate, b_H, err);
   if (e != cudaSuccess) return e;
   const int rows_per_block = 8;
   lmhead_merge_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,
                         stream>>>(partial, static_cast<int>(M), p.n_runs, vals, idx);
   return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead(const uint16_t* hidden, const uint16_t* W, const uint16_t* W_H, const float* b_H,
+                          int64_t M, int64_t V, int64_t d, float* vals, int32_t* idx, float* gate, void* workspace,
+                          int num_sms, uint32_t* err, cudaStream_t stream) {
+  if (d % kBK != 0 || M > 0x7FFFFFFF || d > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  // an even number of 128-row tiles pairs up consecutive row tiles
+  const int64_t m_tiles = (M + 127) / 128;
+  if (m_tiles % 2 == 0)
+    return launch_lmhead_form<true>(hidden, W, W_H, b_H, M, V, d, vals, idx, gate, workspace, num_sms, err, stream);
+  return launch_lmhead_form<false>(hidden, W, W_H, b_H, M, V, d, vals, idx, gate, workspace, num_sms, err, stream);
 }
 
 }  // namespace
