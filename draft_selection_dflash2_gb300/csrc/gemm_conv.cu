@@ -404,12 +404,9 @@ cudaError_t launch_gemm_conv2tap(const uint16_t* A, const uint16_t* W, const uin
       !make_tmap_bf16_2d(&th, hs, M, d, d, 128) || !make_tmap_bf16_2d(&tc, W_c, N, d, d, kGcSubN))
     return cudaErrorInvalidValue;
   const size_t smem = 1024 + kGcStages * kGcStageBytes + sizeof(GcSmem);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gemm_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  {
+    const cudaError_t e = set_smem_limit<gemm_conv_kernel>(smem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   cudaError_t e = cudaMemsetAsync(ga.ready, 0, static_cast<size_t>(ga.m_tiles) * sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;

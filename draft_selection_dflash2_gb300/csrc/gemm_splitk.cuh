@@ -28,6 +28,7 @@
 
 #include <cooperative_groups.h>
 
+#include "launch.h"
 #include "tcgen05.cuh"
 
 namespace dflash2 {
@@ -297,12 +298,9 @@ template <class Epi>
 cudaError_t launch_splitk_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const SplitKShape& sh,
                                const typename Epi::Params& p, uint32_t* err, cudaStream_t stream) {
   const size_t smem = sk_smem_bytes(sh);
-  static size_t configured = 0;
-  if (smem > configured) {
-    const cudaError_t e = cudaFuncSetAttribute(splitk_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
+  {
+    const cudaError_t e = set_smem_limit<splitk_gemm_kernel<Epi>>(smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.ks, sh.n_tiles, sh.m_tiles);

@@ -4,9 +4,45 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "dflash2.h"
 
 namespace dflash2 {
+
+constexpr int kMaxDevices = 64;
+
+// Kernel attributes are per device: these set one for the current device the
+// first time a launch there needs it.  One record per kernel (Fn) and device.
+template <auto Fn>
+cudaError_t set_smem_limit(size_t bytes) {
+  static std::mutex mu;
+  static size_t done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done[dev] = bytes;
+  return e;
+}
+
+template <auto Fn>
+cudaError_t allow_nonportable_clusters() {
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(Fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
 
 int topk_cluster_size(int64_t rows, int64_t V, int num_sms);
 cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, float* vals,

@@ -491,12 +491,9 @@ cudaError_t launch_lmhead_form(const uint16_t* hidden, const uint16_t* W, const 
   const int n_vocab_tiles = static_cast<int>((V + kLmBN - 1) / kLmBN);
   const int64_t Vt = gate ? V + kLmBN : V;
   const size_t smem = 1024 + F::kStages * F::kStageBytes + sizeof(LmSmem);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
+  {
+    const cudaError_t e = set_smem_limit<lmhead_kernel<kPair>>(smem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kLmThreads, 1, 1);
@@ -511,16 +508,22 @@ cudaError_t launch_lmhead_form(const uint16_t* hidden, const uint16_t* W, const 
   cfg.numAttrs = 1;
   int slots = num_sms;
   if (kPair) {
-    // the runs are sized to the pairs that can be resident at once
-    static int resident = 0;
-    if (resident == 0) {
+    // the runs are sized to the pairs that can be resident at once on this device
+    static std::mutex mu;
+    static int resident[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident[dev] == 0) {
       cfg.gridDim = dim3(2, 1, 1);
       int n = 0;
-      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, lmhead_kernel<kPair>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, lmhead_kernel<kPair>, &cfg);
       if (e != cudaSuccess) return e;
-      resident = n > 0 ? n : 1;
+      resident[dev] = n > 0 ? n : 1;
     }
-    slots = 2 * resident;
+    slots = 2 * resident[dev];
   }
   const LmPlan p = lm_plan(M, Vt, slots);
   CUtensorMap ta, tb, th;

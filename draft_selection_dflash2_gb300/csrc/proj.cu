@@ -315,12 +315,9 @@ cudaError_t launch_pair_scores_proj(const int32_t* cand_idx, const float* cand_v
       !make_tmap_bf16_2d(&tb, W_B, kEmbed, d, d, kPjBN))
     return cudaErrorInvalidValue;
   const size_t smem = 1024 + kPjStages * kPjStageBytes + sizeof(PjSmem);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  {
+    const cudaError_t e = set_smem_limit<proj_kernel>(smem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int grid = n_tiles < num_sms ? n_tiles : num_sms;
   proj_kernel<<<grid, kPjThreads, smem, stream>>>(E, ta, tb, cand_idx, last_verified, n_cand, n_rows, V,

@@ -308,11 +308,9 @@ int topk_cluster_size(int64_t rows, int64_t V, int num_sms) {
 cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, float* vals,
                         int32_t* idx, uint32_t* err, int num_sms, cudaStream_t stream) {
   (void)err;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(topk16_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  {
+    const cudaError_t e = allow_nonportable_clusters<topk16_kernel>();
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int S = topk_cluster_size(rows, V, num_sms);
   int64_t seg_len = (V + S - 1) / S;

@@ -667,9 +667,20 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
   const unsigned init_grid = static_cast<unsigned>((rows + 255) / 256);
   verify_init_kernel<<<init_grid, 256, 0, stream>>>(accept_len, reinterpret_cast<uint32_t*>(sc + lay.counters), bar,
                                                    B, L);
-  static int grid_cache[2] = {0, 0};   // per variant; one device per process
-  int& g = grid_cache[sampled ? 1 : 0];
-  if (g == 0) g = max_verify_grid(sampled, num_sms);
+  // the co-resident grid, per device and variant
+  static std::mutex mu;
+  static int grid_cache[kMaxDevices][2] = {};
+  int dev = 0;
+  cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return ge;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int g;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    int& cached = grid_cache[dev][sampled ? 1 : 0];
+    if (cached == 0) cached = max_verify_grid(sampled, num_sms);
+    g = cached;
+  }
   if (g == 0) return cudaErrorInvalidConfiguration;
   const int64_t items = (L + 1) * B * nch;
   const int grid = static_cast<int>(items < g ? items : g);

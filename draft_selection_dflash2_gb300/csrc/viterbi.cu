@@ -102,13 +102,10 @@ cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t
                                 int32_t* draft_slot, float* score, uint32_t* err, cudaStream_t stream) {
   if (L > kViterbiMaxL) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(kViterbiWarps) * viterbi_smem_floats(L) * sizeof(float);
-  static bool configured = false;
-  if (!configured) {
+  {
     const cudaError_t e =
-        cudaFuncSetAttribute(walk_viterbi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kViterbiWarps * viterbi_smem_floats(kViterbiMaxL) * sizeof(float)));
+        set_smem_limit<walk_viterbi_kernel>(kViterbiWarps * viterbi_smem_floats(kViterbiMaxL) * sizeof(float));
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const unsigned grid = static_cast<unsigned>((B + kViterbiWarps - 1) / kViterbiWarps);
   walk_viterbi_kernel<<<grid, kViterbiWarps * 32, smem, stream>>>(S, cand_idx, B, L, draft_tok, draft_slot, score,

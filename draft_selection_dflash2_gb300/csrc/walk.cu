@@ -152,12 +152,9 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
                         int32_t* draft_slot, float* draft_q, uint32_t* err, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kWalkWarps) * walk_smem_floats(L) * sizeof(float);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kWalkWarps * walk_smem_floats(kMaxWalkL) * 4));
+  {
+    const cudaError_t e = set_smem_limit<walk_kernel>(kWalkWarps * walk_smem_floats(kMaxWalkL) * sizeof(float));
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const unsigned grid = static_cast<unsigned>((B + kWalkWarps - 1) / kWalkWarps);
   walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, temperature,
