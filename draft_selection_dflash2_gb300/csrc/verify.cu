@@ -6,25 +6,29 @@
 //
 // Row t of a sequence only matters while every earlier position accepted.  One
 // cooperative launch (all CTAs resident) reads the rows position-major: each
-// target row is cut into contiguous chunks of ids, the (t, b, chunk) items are
-// strided over the grid in that order, and an item is skipped once an earlier
-// position of its sequence is known to have rejected, so only rows within
-// about one position of the decided front are read in vain.  An item leaves its
-// chunk's partial result in scratch:
-//   T = 0: the largest key (value order, then lowest id);
-//   T > 0: the chunk's max and sum of 2^((l - max) c), c = log2(e) / T.
-// The CTA that completes a row's last chunk combines the partials and decides
-// the row:
-//   T = 0: out_tok := arg-max; a mismatch lowers first_reject[b] (atomicMin).
-//   T > 0: accept iff u1 q(x) Z < 2^((l_x - M) c); a rejection lowers
-//          first_reject[b].
-// After a grid barrier, at T > 0, each sequence draws the token of row
-// n = first_reject[b]: from the residual max(0, e_v - q_v Z) after a rejection,
-// from p itself for the bonus row n = L; in id order, the chunk by its mass,
-// then inside the chunk (re-read) a run of vectors, a vector and an id.  After a
-// last barrier: out_tok = draft[0..n-1], row n's token, -1...; accept_len[b] =
-// n + 1.  Every barrier wait is bounded (2 s, then DFLASH2_DEVERR_TIMEOUT and
-// every CTA stops).
+// target row is cut into contiguous chunks of about 4096 ids, one warp's item,
+// and the (t, chunk, b) items are strided over all warps of the grid in that
+// order (sequences fastest, so that each sequence's work is spread over SMs).  A row is dead once an earlier position of its sequence is known to
+// have rejected (first_reject only falls, so a dead row stays dead); a warp
+// checks its next 32 items at once, with the loads of the first already in
+// flight, and skips the dead ones.  Rows within about one position of the
+// decided front are read in vain.
+//   T = 0: the row's arg-max key (value order, then lowest id) is kept by a
+//          64-bit atomic max per row; a chunk holding a key above the draft
+//          token's rejects the row at once (atomicMin on first_reject), so no
+//          chunk waits for another.  After a grid barrier, row n's key gives
+//          its token.
+//   T > 0: each chunk leaves its max and sum of 2^((l - max) c), c = log2(e) / T,
+//          in scratch; the warp that completes a row's last chunk combines them
+//          and tests u1 q(x) Z < 2^((l_x - M) c); a rejection lowers
+//          first_reject[b].  After a grid barrier each sequence draws the token
+//          of row n = first_reject[b]: from the residual max(0, e_v - q_v Z)
+//          after a rejection, from p itself for the bonus row n = L; in id
+//          order, the chunk by its mass, then inside the chunk (re-read) a run
+//          of vectors, a vector and an id.
+// After a last barrier: out_tok = draft[0..n-1], row n's token, -1...;
+// accept_len[b] = n + 1.  Every barrier wait is bounded (2 s, then
+// DFLASH2_DEVERR_TIMEOUT and every CTA stops).
 #include "common.cuh"
 #include "launch.h"
 #include "philox.cuh"
@@ -34,38 +38,40 @@ namespace {
 
 constexpr int kVThreads = 256;
 constexpr int kVWarps = kVThreads / 32;
-constexpr int kVUnroll = 8;          // 16-byte loads in flight per thread
-constexpr int kChunks = 4;           // chunks per target row (more if one would exceed kDrawVecs vectors)
+constexpr int kVUnroll = 8;          // 16-byte loads in flight per lane
+constexpr int kChunkIds = 4096;      // target ids per chunk (one warp's item)
 constexpr int kVCtasPerSm = 4;          // T = 0 (64 registers)
 constexpr int kVCtasPerSmSampled = 3;   // T > 0 (85 registers)
 constexpr int kDrawVecs = 5120;      // largest chunk a draw handles: 40960 ids
-constexpr int kMaxChunks = kVThreads; // chunks per row the decisions combine in one step (V < 10.5M)
+constexpr int kMaxChunks = kVThreads; // chunks per row the draws combine in one step (V < 10.5M)
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct alignas(8) ChunkPartial {
-  float m;          // T > 0: the chunk's largest logit
+struct alignas(16) ChunkPartial {
+  float m;          // the chunk's largest logit
   uint32_t pad;
-  double z;         // T > 0: sum over the chunk of 2^((l - m) c)
-  uint64_t key;     // T = 0: (value order << 32) | ~id, 0 if the chunk is empty
+  double z;         // sum over the chunk of 2^((l - m) c)
 };
 
-
-// Chunks per row and ids per chunk (a multiple of 8, at most kDrawVecs vectors).
+// Chunks per row (about kChunkIds ids each, at most kMaxChunks) and ids per
+// chunk (a multiple of 8, at most kDrawVecs vectors while V < 10.5M).
 __host__ __device__ inline int verify_chunks(int64_t V) {
-  const int64_t by_draw = (V + kDrawVecs * 8 - 1) / (kDrawVecs * 8);
-  return static_cast<int>(by_draw > kChunks ? by_draw : kChunks);
+  int64_t n = (V + kChunkIds - 1) / kChunkIds;
+  if (n < 1) n = 1;
+  if (n > kMaxChunks) n = kMaxChunks;
+  return static_cast<int>(n);
 }
 __host__ __device__ inline int64_t verify_chunk_ids(int64_t V) {
   const int n = verify_chunks(V);
   return (((V + n - 1) / n) + 7) & ~int64_t(7);
 }
 
-// scratch layout: barrier words | arrival counters [rows] | partials [rows, chunks]
+// scratch layout: barrier words | arrival counters [rows] | row keys [rows] | partials [rows, chunks]
 struct ScratchLayout {
-  size_t counters, partials, total;
+  size_t counters, keys, partials, total;
   __host__ __device__ ScratchLayout(int64_t rows, int nch) {
     counters = 256;
-    partials = counters + ((static_cast<size_t>(rows) * 4 + 255) / 256) * 256;
+    keys = counters + ((static_cast<size_t>(rows) * 4 + 255) / 256) * 256;
+    partials = keys + ((static_cast<size_t>(rows) * 8 + 255) / 256) * 256;
     total = partials + static_cast<size_t>(rows) * nch * sizeof(ChunkPartial);
   }
 };
@@ -106,8 +112,7 @@ __device__ __forceinline__ double warp_sum_f64(double x) {
 }
 
 struct VerifySmem {
-  int last, abort, skip[2];
-  uint64_t key[kVWarps];
+  int abort;
   float m[kVWarps];
   double z[kVWarps];
   // draws
@@ -120,73 +125,91 @@ struct VerifySmem {
   double candr[kTopK];        // candidate residual max(0, e - q Z)
   double runs[kVThreads];     // draw: mass of each thread's run of vectors
   double pmass[kMaxChunks];   // the row's chunk masses relative to the row max
-  uint32_t lx;                // accept test: the draft token's logit bits
   float vmass[kDrawVecs];     // draw: mass of each 8-id vector of the chunk
 };
 
-__device__ uint64_t block_max_key(VerifySmem& s, uint64_t k) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) k = kmax(k, __shfl_xor_sync(0xFFFFFFFFu, k, o));
-  if (lane == 0) s.key[warp] = k;
-  __syncthreads();
-  uint64_t r = s.key[0];
+  return k;
+}
+
+__device__ __forceinline__ float warp_max_f32(float x) {
 #pragma unroll
-  for (int w = 1; w < kVWarps; ++w) r = kmax(r, s.key[w]);
-  __syncthreads();
-  return r;
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+// An id's key: (value order << 32) | ~id, so that the largest key is the
+// largest value and, among equal values, the lowest id; NaN orders below -inf
+// (ranked among themselves by id), -0 equals +0.
+__device__ __forceinline__ uint64_t id_key(uint32_t bits, uint32_t id) {
+  return (static_cast<uint64_t>(bf16_order(bits)) << 32) | static_cast<uint64_t>(~id);
 }
 
 // ---------------------------------------------------------------------------
-// one chunk [v0, v1) of a row (v0 % 8 == 0)
+// one chunk [v0, v1) of a row (v0 % 8 == 0), one warp
 // ---------------------------------------------------------------------------
-// Largest key of the chunk: (value order << 32) | ~id, so the lowest id wins ties.
-// The stream keeps, per thread, only the best vector maximum and the first
-// vector holding it (a strict > in the thread's increasing vector order keeps
-// the first); the thread then re-reads that one vector to name the lowest id
-// with that value.  NaN orders below -inf and never becomes a best (an all-NaN
-// chunk gives key 0).
+// The chunk's vectors are read in batches of U per lane (lane + 32 u, in
+// increasing order per lane).  The caller issues the first batch (load_batch)
+// before it knows whether the item is live, so that the check's loads and the
+// data's are in flight together.
 template <int U>
-__device__ uint64_t chunk_argmax(const uint16_t* row, int64_t v0, int64_t v1) {
-  const uint4* rv = reinterpret_cast<const uint4*>(row + v0);
-  const int64_t nvec = (v1 - v0) >> 3;
-  uint32_t best = 0u;       // value order of the best vector maximum (0: none yet)
-  int64_t best_vec = -1;
-  for (int64_t i = threadIdx.x; i < nvec; i += U * kVThreads) {
-    uint4 v[U];
+__device__ __forceinline__ void load_batch(uint4 (&v)[U], const uint4* rv, int base, int nvec, int lane) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) v[u] = i + u * kVThreads < nvec ? ldg_stream(rv + i + u * kVThreads) : make_uint4(0, 0, 0, 0);
+  for (int u = 0; u < U; ++u) {
+    const int i = base + lane + 32 * u;
+    v[u] = i < nvec ? ldg_stream(rv + i) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Largest key of the chunk.  Each lane keeps its best vector maximum, the
+// first vector holding it (a strict > in increasing vector order keeps the
+// first; a lane's first vector starts as best even if all NaN) and that
+// vector's data, then names the lowest id with that value; the warp takes the
+// largest key.  0 only for an empty chunk.  v holds the first batch on entry.
+template <int U>
+__device__ __forceinline__ uint64_t warp_chunk_argmax(uint4 (&v)[U], const uint4* rv, int64_t v0, int64_t v1, const uint16_t* row,
+                                      int lane) {
+  const int nvec = static_cast<int>((v1 - v0) >> 3);
+  uint32_t best = 0u;
+  int best_i = -1;
+  uint4 bestv = make_uint4(0, 0, 0, 0);
+  for (int base = 0;;) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t vo = i + u * kVThreads < nvec ? bf16_order(vec_max_bits(v[u])) : 0u;
-      const bool better = vo > best;
-      best = better ? vo : best;
-      best_vec = better ? i + u * kVThreads : best_vec;
+      const int i = base + lane + 32 * u;
+      if (i < nvec) {
+        const uint32_t vo = bf16_order(vec_max_bits(v[u]));
+        const bool better = best_i < 0 || vo > best;
+        best = better ? vo : best;
+        best_i = better ? i : best_i;
+        bestv = better ? v[u] : bestv;
+      }
     }
+    base += 32 * U;
+    if (base >= nvec) break;
+    load_batch<U>(v, rv, base, nvec, lane);
   }
   uint64_t key = 0ull;
-  if (best_vec >= 0) {
-    const uint4 v = rv[best_vec];
-    const uint32_t id0 = static_cast<uint32_t>(v0 + best_vec * 8);
+  if (best_i >= 0) {
+    const uint32_t id0 = static_cast<uint32_t>(v0 + static_cast<int64_t>(best_i) * 8);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      key = kmax(key, (static_cast<uint64_t>(bf16_order(lane_bits(v, k))) << 32) | static_cast<uint64_t>(~(id0 + k)));
+    for (int k = 0; k < 8; ++k) key = kmax(key, id_key(lane_bits(bestv, k), id0 + k));
   }
-  for (int64_t e = v0 + nvec * 8 + threadIdx.x; e < v1; e += kVThreads)
-    key = kmax(key, (static_cast<uint64_t>(bf16_order(row[e])) << 32) |
-                        static_cast<uint64_t>(~static_cast<uint32_t>(e)));
-  return key;
+  for (int64_t e = v0 + static_cast<int64_t>(nvec) * 8 + lane; e < v1; e += 32)
+    key = kmax(key, id_key(row[e], static_cast<uint32_t>(e)));
+  return warp_max_u64(key);
 }
 
 // Softmax statistics of the chunk at inverse temperature c: its max m and
-// z = sum 2^((l - m) c).  Per thread a running max and a Kahan-compensated fp32
-// sum of per-vector fp32 sums (~1e-7 relative); the block combines in fp64.
+// z = sum 2^((l - m) c).  Per lane a running max and a Kahan-compensated fp32
+// sum of per-vector fp32 sums (~1e-7 relative); the warp combines in fp64.
+// Every lane returns m and z.  v holds the first batch on entry.
 template <int U>
-__device__ void chunk_stats(VerifySmem& s, const uint16_t* row, int64_t v0, int64_t v1, float c, float* m_out,
-                            double* z_out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint4* rv = reinterpret_cast<const uint4*>(row + v0);
-  const int64_t nvec = (v1 - v0) >> 3;
+__device__ __forceinline__ void warp_chunk_stats(uint4 (&v)[U], const uint4* rv, int64_t v0, int64_t v1, const uint16_t* row,
+                                 float c, int lane, float* m_out, double* z_out) {
+  const int nvec = static_cast<int>((v1 - v0) >> 3);
   float m = -INFINITY;
   float acc = 0.0f, comp = 0.0f;
   auto add = [&](float x) {
@@ -195,64 +218,67 @@ __device__ void chunk_stats(VerifySmem& s, const uint16_t* row, int64_t v0, int6
     comp = (t2 - acc) - y;
     acc = t2;
   };
-  auto absorb = [&](const uint4& v) {
-    const float vm = bf16_bits_to_float(vec_max_bits(v));
-    if (vm > m) {
-      const float r = fast_exp2((m - vm) * c);
-      acc *= r;
-      comp *= r;
-      m = vm;
-    }
-    const float mc = m * c;
-    float vs = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) vs += fast_exp2(fmaf(bf16_bits_to_float(lane_bits(v, k)), c, -mc));
-    add(vs);
+  auto rescale = [&](float nm) {
+    const float r = fast_exp2((m - nm) * c);
+    acc *= r;
+    comp *= r;
+    m = nm;
   };
-  // every batch (the last, partial one included) has all its loads in flight at once
-  for (int64_t i = threadIdx.x; i < nvec; i += U * kVThreads) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) v[u] = i + u * kVThreads < nvec ? ldg_stream(rv + i + u * kVThreads) : make_uint4(0, 0, 0, 0);
+  for (int base = 0;;) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (i + u * kVThreads >= nvec) break;
-      absorb(v[u]);
+      if (base + lane + 32 * u < nvec) {
+        const float vm = bf16_bits_to_float(vec_max_bits(v[u]));
+        if (vm > m) rescale(vm);
+        const float mc = m * c;
+        float e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = fast_exp2(fmaf(bf16_bits_to_float(lane_bits(v[u], k)), c, -mc));
+        add(((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
+      }
     }
+    base += 32 * U;
+    if (base >= nvec) break;
+    load_batch<U>(v, rv, base, nvec, lane);
   }
-  for (int64_t e = v0 + nvec * 8 + threadIdx.x; e < v1; e += kVThreads) {
+  for (int64_t e = v0 + static_cast<int64_t>(nvec) * 8 + lane; e < v1; e += 32) {
     const float x = bf16_bits_to_float(row[e]);
-    if (x > m) {
-      const float r = fast_exp2((m - x) * c);
-      acc *= r;
-      comp *= r;
-      m = x;
-    }
+    if (x > m) rescale(x);
     add(fast_exp2((x - m) * c));
   }
-  float wm = m;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
-  if (lane == 0) s.m[warp] = wm;
-  __syncthreads();
-  float M = s.m[0];
-#pragma unroll
-  for (int w = 1; w < kVWarps; ++w) M = fmaxf(M, s.m[w]);
+  const float M = warp_max_f32(m);
   double z = (m == -INFINITY) ? 0.0
                               : (static_cast<double>(acc) - static_cast<double>(comp)) *
                                     static_cast<double>(fast_exp2((m - M) * c));
-  z = warp_sum_f64(z);
-  if (lane == 0) s.z[warp] = z;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double Z = 0.0;
-    for (int w = 0; w < kVWarps; ++w) Z += s.z[w];
-    *m_out = M;
-    *z_out = Z;
-  }
-  __syncthreads();
+  *m_out = M;
+  *z_out = warp_sum_f64(z);
 }
 
+
+// Inclusive fp64 prefix sum over the warp's lanes (every lane calls).
+__device__ __forceinline__ double warp_scan_incl(double x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Inverse-CDF pick over lanes in order, lane j holding mass w_j >= 0 and
+// incl_j = sum_{i <= j} w_i: the first lane with w > 0 whose inclusive mass
+// passes target, else (rounding) the last lane with w > 0, else -1.  *before
+// gets the picked lane's exclusive prefix (0 if none).  Every lane calls.
+__device__ __forceinline__ int warp_pick(double w, double incl, double target, int lane, double* before) {
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, w > 0.0 && target < incl);
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.0);
+  const int src = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (lane == 0) excl = 0.0;
+  const double b = __shfl_sync(0xFFFFFFFFu, excl, src < 0 ? 0 : src);
+  *before = src < 0 ? 0.0 : b;
+  return src;
+}
 
 // ---------------------------------------------------------------------------
 // drawing inside one chunk
@@ -344,46 +370,33 @@ __device__ int32_t chunk_draw(VerifySmem& s, const uint16_t* row, int64_t v0, in
         if (k == pk) b = pe + (k > 0 ? lk[k - 1] : 0.0);
       before = b;
     }
-    if (lane == 0) {
-      s.pick = pick;
-      s.target = target - before;
-    }
-  }
-  __syncthreads();
-  if (tid == s.pick) {
-    // the run's vectors, then the picked vector's ids (candidates at their residual);
-    // without a hit (rounding) the last vector and id of positive weight
-    double run = 0.0, vec_base = 0.0;
-    int vec = -1;
-    for (int i = tid * per; i < nv && i < (tid + 1) * per; ++i) {
-      const double m = fmaxf(s.vmass[i], 0.0f);
-      if (m > 0.0) {
-        vec = i;
-        vec_base = run;
-        if (s.target < run + m) break;
-      }
-      run += m;
-    }
-    int32_t tok = -1, last_pos = -1;
-    if (vec >= 0) {
-      double r2 = vec_base;
-      const int64_t a = v0 + static_cast<int64_t>(vec) * 8, e = a + 8 < v1 ? a + 8 : v1;
-      const uint4 x = a + 8 <= v1 ? *reinterpret_cast<const uint4*>(row + a) : make_uint4(0, 0, 0, 0);
-      for (int64_t v = a; v < e; ++v) {
-        double w = a + 8 <= v1 ? static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(lane_bits(x, static_cast<int>(v - a))), c, -mc)))
-                               : static_cast<double>(weight(v));
-        for (int q = 0; q < n_cand; ++q)
-          if (s.cand[q] == v) w = s.candr[q];
-        if (w > 0.0) {
-          last_pos = static_cast<int32_t>(v);
-          r2 += w;
-          if (tok < 0 && s.target < r2) tok = static_cast<int32_t>(v);
+    // the run's vectors (lane j: vector pick * per + j), then the picked
+    // vector's ids (lane k: id a + k, a candidate at its residual); without a
+    // hit (rounding) the last vector and id of positive weight
+    int32_t token = static_cast<int32_t>(v0);
+    if (pick >= 0) {
+      const double tgt = target - before;
+      const int i = pick * per + lane;
+      const double m = lane < per && i < nv ? static_cast<double>(fmaxf(s.vmass[i], 0.0f)) : 0.0;
+      double vec_base;
+      const int vj = warp_pick(m, warp_scan_incl(m, lane), tgt, lane, &vec_base);
+      if (vj >= 0) {
+        const int64_t id = v0 + static_cast<int64_t>(pick * per + vj) * 8 + lane;
+        double w = 0.0;
+        if (lane < 8 && id < v1) {
+          w = static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(row[id]), c, -mc)));
+          for (int q = 0; q < n_cand; ++q)
+            if (s.cand[q] == id) w = s.candr[q];
         }
+        const double incl_w = warp_scan_incl(w, lane);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, w > 0.0 && tgt < vec_base + incl_w);
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.0);
+        if (hit) token = static_cast<int32_t>(v0 + static_cast<int64_t>(pick * per + vj) * 8 + __ffs(hit) - 1);
+        else if (pos) token = static_cast<int32_t>(v0 + static_cast<int64_t>(pick * per + vj) * 8 + 31 - __clz(pos));
       }
     }
-    s.token = tok >= 0 ? tok : (last_pos >= 0 ? last_pos : static_cast<int32_t>(v0));
+    if (lane == 0) s.token = token;
   }
-  if (s.pick < 0 && tid == 0) s.token = static_cast<int32_t>(v0);
   __syncthreads();
   return s.token;
 }
@@ -460,11 +473,15 @@ __device__ void grid_barrier(unsigned* count, volatile unsigned* gen, volatile u
 // ---------------------------------------------------------------------------
 // kernels
 // ---------------------------------------------------------------------------
-__global__ void verify_init_kernel(int32_t* first_reject, uint32_t* counters, unsigned* bar, int64_t B, int64_t L) {
+__global__ void verify_init_kernel(int32_t* first_reject, uint32_t* counters, unsigned long long* keys, unsigned* bar,
+                                   int64_t B, int64_t L) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t rows = B * (L + 1);
   if (i < B) first_reject[i] = static_cast<int32_t>(L);
-  if (i < rows) counters[i] = 0u;
+  if (i < rows) {
+    counters[i] = 0u;
+    keys[i] = 0ull;
+  }
   if (i < 4) bar[i] = 0u;   // count, generation, abort
 }
 
@@ -480,11 +497,80 @@ struct VerifyArgs {
   uint64_t seed, offset;
   int32_t* first_reject;   // = accept_len until the end
   int32_t* out_tok;
-  uint32_t* counters;
-  ChunkPartial* partials;
+  uint32_t* counters;      // T > 0: chunks completed per row
+  unsigned long long* keys;   // T = 0: the row's largest key
+  ChunkPartial* partials;  // T > 0: [rows, chunks]
   unsigned* bar;           // [0] count, [1] generation, [2] abort
   uint32_t* err;
 };
+
+// T > 0, the warp that completed row (b, t): the row's max M and Z from its
+// chunk partials (lane q reads chunks q, q + 32, ...; fixed order, fp64), then
+// the accept test u1 q(x) Z < 2^((l_x - M) c); a rejection lowers first_reject[b].
+__device__ void decide_sampled_row(const VerifyArgs& a, const ChunkPartial* part, int nch, const uint16_t* row,
+                                   int64_t b, int64_t t, float c, int lane) {
+  const int64_t L = a.L;
+  if (t >= L) return;   // the bonus row has no test
+  int32_t f = 0;
+  if (lane == 0) f = *reinterpret_cast<volatile int32_t*>(a.first_reject + b);
+  if (t > __shfl_sync(0xFFFFFFFFu, f, 0)) return;   // past a known rejection (warp-uniform)
+  uint32_t lx = 0u;
+  int32_t slot = 0;
+  if (lane == 0) {
+    lx = row[clamp_token(a.draft_tok[b * L + t], a.V, a.err)];   // in flight with the partials
+    slot = a.draft_slot[b * L + t];
+  }
+  constexpr int kPer = kMaxChunks / 32;
+  float mq[kPer];
+  double zq[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int q = lane + 32 * k;
+    mq[k] = -INFINITY;
+    zq[k] = 0.0;
+    if (q < nch) {
+      mq[k] = __ldcg(&part[q].m);
+      zq[k] = __ldcg(&part[q].z);
+    }
+  }
+  float ml = mq[0];
+#pragma unroll
+  for (int k = 1; k < kPer; ++k) ml = fmaxf(ml, mq[k]);
+  const float M = warp_max_f32(ml);
+  double zl = 0.0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    if (mq[k] != -INFINITY) zl += zq[k] * static_cast<double>(fast_exp2((mq[k] - M) * c));
+  const double Z = warp_sum_f64(zl);
+  if (lane == 0) {
+    if (slot < 0 || slot >= kTopK) {
+      raise_error(a.err, DFLASH2_DEVERR_BAD_SLOT);
+      slot = slot < 0 ? 0 : kTopK - 1;
+    }
+    const double q = static_cast<double>(a.draft_q[(b * L + t) * kTopK + slot]);
+    const double ex = static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(lx), c, -M * c)));
+    const double u1 = philox_uniform24(a.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 1, a.offset);
+    if (!(u1 * q * Z < ex)) atomicMin(a.first_reject + b, static_cast<int32_t>(t));
+  }
+}
+
+// A work item's (position, sequence, chunk).
+struct ItemPos {
+  int t, b, ch;
+};
+
+// p + d for d's components below their moduli (b < B, ch < nch): one carry each.
+__device__ __forceinline__ ItemPos item_add(ItemPos p, ItemPos d, int nch, int B) {
+  ItemPos r;
+  r.b = p.b + d.b;
+  const int c1 = r.b >= B;
+  r.b -= c1 ? B : 0;
+  r.ch = p.ch + d.ch + c1;
+  const int c2 = r.ch >= nch;
+  r.ch -= c2 ? nch : 0;
+  r.t = p.t + d.t + c2;
+  return r;
+}
 
 template <bool kSampled>
 __global__ void __launch_bounds__(kVThreads, kSampled ? kVCtasPerSmSampled : kVCtasPerSm)
@@ -495,80 +581,84 @@ __global__ void __launch_bounds__(kVThreads, kSampled ? kVCtasPerSmSampled : kVC
   const int64_t cs = verify_chunk_ids(V);
   const float c = kSampled ? kLog2e / a.temperature : 0.0f;
   volatile int32_t* fr = a.first_reject;
+  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s.abort = 0;
   __syncthreads();
   {
-    const int64_t items = (L + 1) * B * nch;
-    int parity = 0;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, parity ^= 1) {
-      const int64_t t = item / (B * nch), b = (item / nch) % B;
-      const int ch = static_cast<int>(item % nch);
-      // a row past a known rejection is skipped; thread 0 decides for the whole CTA
-      // (first_reject may change under it), through a slot that alternates with the
-      // item so that one barrier suffices
-      if (threadIdx.x == 0) s.skip[parity] = t > fr[b] ? 1 : 0;
-      __syncthreads();
-      if (s.skip[parity]) continue;
-      const int64_t ri = b * (L + 1) + t;
+    // item = (t * nch + ch) * B + b: position-major, the sequence fastest, so a
+    // sequence's chunks fall on warps of different CTAs (and SMs) and the work
+    // of the sequences still alive stays spread over the GPU.  Positions are
+    // stepped by carry-adds of precomputed (t, ch, b) offsets, so the loop
+    // divides nothing.
+    const int64_t per_pos = B * nch;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kVWarps;
+    auto split = [&](int64_t x) {
+      ItemPos p;
+      p.t = static_cast<int>(x / per_pos);
+      const int64_t r = x % per_pos;
+      p.ch = static_cast<int>(r / B);
+      p.b = static_cast<int>(r % B);
+      return p;
+    };
+    const int Bi = static_cast<int>(B);
+    const ItemPos stride = split(nwarps), ahead = split(lane * nwarps);
+    ItemPos cur = split(static_cast<int64_t>(blockIdx.x) * kVWarps + (threadIdx.x >> 5));
+    while (cur.t <= L) {
+      const int t = cur.t, b = cur.b, ch = cur.ch;
+      const int64_t ri = static_cast<int64_t>(b) * (L + 1) + t;
       const uint16_t* row = a.target + ri * a.ld;
       const int64_t v0 = ch * cs < V ? ch * cs : V, v1 = v0 + cs < V ? v0 + cs : V;
-      ChunkPartial* out = a.partials + ri * nch + ch;
+      const uint4* rv = reinterpret_cast<const uint4*>(row + v0);
+      const int nvec = static_cast<int>((v1 - v0) >> 3);
+      // the first batch, then (with it in flight) whether this item and the
+      // warp's next 31 are live
+      uint4 v[kVUnroll];
+      load_batch<kVUnroll>(v, rv, 0, nvec, lane);
+      int32_t dt = -1;
+      uint32_t dbits = 0u;
+      if (!kSampled && lane == 0 && t < L) {
+        dt = a.draft_tok[static_cast<int64_t>(b) * L + t];
+        if (dt >= 0 && dt < V) dbits = row[dt];
+      }
+      const ItemPos mine = item_add(cur, ahead, nch, Bi);
+      const bool live = mine.t <= L && mine.t <= fr[mine.b];
+      const unsigned mask = __ballot_sync(0xFFFFFFFFu, live);
+      if (!(mask & 1u)) {
+        // the first live one of the 32, else the one after them
+        const int k = mask ? __ffs(mask) - 1 : 31;
+        cur.t = __shfl_sync(0xFFFFFFFFu, mine.t, k);
+        cur.b = __shfl_sync(0xFFFFFFFFu, mine.b, k);
+        cur.ch = __shfl_sync(0xFFFFFFFFu, mine.ch, k);
+        if (!mask) cur = item_add(cur, stride, nch, Bi);
+        continue;
+      }
       if (!kSampled) {
-        const uint64_t key = block_max_key(s, chunk_argmax<kVUnroll>(row, v0, v1));
-        if (threadIdx.x == 0) out->key = key;
+        const uint64_t key = warp_chunk_argmax<kVUnroll>(v, rv, v0, v1, row, lane);
+        if (lane == 0) {
+          if (key) atomicMax(a.keys + ri, static_cast<unsigned long long>(key));
+          // a key above the draft token's rejects the row (an id outside [0, V)
+          // is never the arg-max)
+          if (t < L && (dt < 0 || dt >= V || key > id_key(dbits, static_cast<uint32_t>(dt))))
+            atomicMin(a.first_reject + b, static_cast<int32_t>(t));
+        }
       } else {
         float m;
         double z;
-        chunk_stats<kVUnroll>(s, row, v0, v1, c, &m, &z);
-        if (threadIdx.x == 0) {
-          out->m = m;
-          out->z = z;
+        warp_chunk_stats<kVUnroll>(v, rv, v0, v1, row, c, lane, &m, &z);
+        ChunkPartial* part = a.partials + ri * nch;
+        uint32_t prev = 0u;
+        if (lane == 0) {
+          part[ch].m = m;
+          part[ch].z = z;
+          __threadfence();
+          prev = atomicAdd(a.counters + ri, 1u);
+        }
+        if (__shfl_sync(0xFFFFFFFFu, prev, 0) == static_cast<uint32_t>(nch - 1)) {
+          __threadfence();
+          decide_sampled_row(a, part, nch, row, b, t, c, lane);
         }
       }
-      if (threadIdx.x == 0) {
-        __threadfence();
-        s.last = (atomicAdd(a.counters + ri, 1u) == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
-      }
-      __syncthreads();
-      if (!s.last) continue;
-      // the row's last chunk: decide it
-      const ChunkPartial* part = a.partials + ri * nch;
-      __threadfence();
-      if (!kSampled) {
-        uint64_t key = 0ull;
-        for (int q = threadIdx.x; q < nch; q += kVThreads)
-          key = kmax(key, __ldcg(reinterpret_cast<const unsigned long long*>(&part[q].key)));
-        key = block_max_key(s, key);
-        if (threadIdx.x == 0) {
-          // an all-NaN row never sets a key: its arg-max is the lowest id, 0
-          const int32_t tok = key == 0ull ? 0 : static_cast<int32_t>(~static_cast<uint32_t>(key));
-          a.out_tok[ri] = tok;
-          if (t < L && a.draft_tok[b * L + t] != tok) atomicMin(a.first_reject + b, static_cast<int32_t>(t));
-        }
-        __syncthreads();
-        continue;
-      }
-      if (threadIdx.x == kVThreads - 1 && t < L)
-        s.lx = row[clamp_token(a.draft_tok[b * L + t], V, a.err)];   // in flight with the partials
-      combine_row(s, part, nch, c);
-      if (threadIdx.x == 0) {
-        const float M = s.row_max;
-        const double Z = s.row_z;
-        if (t < L && t <= fr[b]) {
-          // accept test: u1 q(x) Z < 2^((l_x - M) c)
-          int32_t slot = a.draft_slot[b * L + t];
-          if (slot < 0 || slot >= kTopK) {
-            raise_error(a.err, DFLASH2_DEVERR_BAD_SLOT);
-            slot = slot < 0 ? 0 : kTopK - 1;
-          }
-          const double q = static_cast<double>(a.draft_q[(b * L + t) * kTopK + slot]);
-          const double ex = static_cast<double>(fast_exp2(fmaf(bf16_bits_to_float(s.lx), c, -M * c)));
-          const double u1 =
-              philox_uniform24(a.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(t), 1, a.offset);
-          if (!(u1 * q * Z < ex)) atomicMin(a.first_reject + b, static_cast<int32_t>(t));
-        }
-      }
-      __syncthreads();
+      cur = item_add(cur, stride, nch, Bi);
     }
     grid_barrier(a.bar, a.bar + 1, a.bar + 2, s, a.err);
   }
@@ -597,40 +687,67 @@ __global__ void __launch_bounds__(kVThreads, kSampled ? kVCtasPerSmSampled : kVC
         atomicAdd(&s.pmass[q], s.candr[threadIdx.x] - s.cande[threadIdx.x]);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        double total_mass = 0.0;
-        for (int q = 0; q < nch; ++q) total_mass += s.pmass[q] > 0.0 ? s.pmass[q] : 0.0;
+      if (threadIdx.x < 32) {
+        // warp 0: the chunk by its mass (inverse CDF in id order); lane j sums
+        // chunks [j k, j k + k), the picked lane finds the chunk among its own
+        const int k = (nch + 31) >> 5;
+        double lsum = 0.0;
+        for (int i = 0; i < k; ++i) {
+          const int q = lane * k + i;
+          if (q < nch) lsum += s.pmass[q] > 0.0 ? s.pmass[q] : 0.0;
+        }
+        const double incl = warp_scan_incl(lsum, lane);
+        const double total_mass = __shfl_sync(0xFFFFFFFFu, incl, 31);
         const double u2 = philox_uniform24(a.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 2, a.offset);
         const double tgt = u2 * total_mass;
-        double run = 0.0, before = 0.0;
-        int pick = -1;
-        for (int q = 0; q < nch; ++q) {
-          const double pq = s.pmass[q] > 0.0 ? s.pmass[q] : 0.0;
-          if (pq > 0.0) {
-            pick = q;
-            before = run;
-            if (tgt < run + pq) break;
+        double lane_before;
+        const int src = warp_pick(lsum, incl, tgt, lane, &lane_before);
+        if (lane == (src < 0 ? 0 : src)) {
+          double run = lane_before, before = 0.0;
+          int pick = -1;
+          for (int i = 0; src >= 0 && i < k; ++i) {
+            const int q = lane * k + i;
+            if (q >= nch) break;
+            const double pq = s.pmass[q] > 0.0 ? s.pmass[q] : 0.0;
+            if (pq > 0.0) {
+              pick = q;
+              before = run;
+              if (tgt < run + pq) break;
+            }
+            run += pq;
           }
-          run += pq;
+          s.pick = pick < 0 ? 0 : pick;
+          s.target = tgt - before;
         }
-        s.pick = pick < 0 ? 0 : pick;
-        s.target = tgt - before;
       }
       __syncthreads();
       const int64_t d0 = s.pick * cs < V ? s.pick * cs : V, d1 = d0 + cs < V ? d0 + cs : V;
       const int32_t tok = chunk_draw(s, row, d0, d1, c, n_cand);
-      if (threadIdx.x == 0) a.out_tok[ri] = tok;
-      __syncthreads();
+      // this sequence's outputs: the accepted prefix, row n's token, then -1
+      for (int64_t t = threadIdx.x; t <= L; t += kVThreads)
+        a.out_tok[b * (L + 1) + t] = t < n ? a.draft_tok[b * L + t] : (t == n ? tok : -1);
+      __syncthreads();   // every thread has read first_reject[b]
+      if (threadIdx.x == 0) a.first_reject[b] = static_cast<int32_t>(n + 1);
     }
-    grid_barrier(a.bar, a.bar + 1, a.bar + 2, s, a.err);
+    return;
   }
+  if (kSampled) return;   // a barrier gave up: DFLASH2_DEVERR_TIMEOUT is raised
   // n = first_reject[b]: the accepted prefix, row n's token, then -1
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < B; b += stride) {
     const int32_t n = fr[b];
     for (int64_t t = 0; t <= L; ++t) {
-      if (t < n) a.out_tok[b * (L + 1) + t] = a.draft_tok[b * L + t];
-      else if (t > n) a.out_tok[b * (L + 1) + t] = -1;
+      if (t < n) {
+        a.out_tok[b * (L + 1) + t] = a.draft_tok[b * L + t];
+      } else if (t == n) {
+        if (!kSampled) {
+          // row n's largest key (an all-NaN row's is its lowest id's, so 0 only if empty)
+          const unsigned long long key = __ldcg(a.keys + b * (L + 1) + t);
+          a.out_tok[b * (L + 1) + t] = key ? static_cast<int32_t>(~static_cast<uint32_t>(key)) : 0;
+        }
+      } else {
+        a.out_tok[b * (L + 1) + t] = -1;
+      }
     }
     a.first_reject[b] = n + 1;
   }
@@ -665,8 +782,8 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   unsigned* bar = reinterpret_cast<unsigned*>(sc);
   const unsigned init_grid = static_cast<unsigned>((rows + 255) / 256);
-  verify_init_kernel<<<init_grid, 256, 0, stream>>>(accept_len, reinterpret_cast<uint32_t*>(sc + lay.counters), bar,
-                                                   B, L);
+  verify_init_kernel<<<init_grid, 256, 0, stream>>>(accept_len, reinterpret_cast<uint32_t*>(sc + lay.counters),
+                                                   reinterpret_cast<unsigned long long*>(sc + lay.keys), bar, B, L);
   // the co-resident grid, per device and variant
   static std::mutex mu;
   static int grid_cache[kMaxDevices][2] = {};
@@ -682,12 +799,12 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
     g = cached;
   }
   if (g == 0) return cudaErrorInvalidConfiguration;
-  const int64_t items = (L + 1) * B * nch;
-  const int grid = static_cast<int>(items < g ? items : g);
+  const int64_t ctas = ((L + 1) * B * nch + kVWarps - 1) / kVWarps;   // one warp per item at most
+  const int grid = static_cast<int>(ctas < g ? ctas : g);
   VerifyArgs args{target, ld, draft_tok, draft_slot, draft_q, cand_idx, B, L, V, temperature, seed, offset,
                   accept_len, out_tok, reinterpret_cast<uint32_t*>(sc + lay.counters),
-                  reinterpret_cast<ChunkPartial*>(sc + lay.partials),
-                  bar, err};
+                  reinterpret_cast<unsigned long long*>(sc + lay.keys),
+                  reinterpret_cast<ChunkPartial*>(sc + lay.partials), bar, err};
   void* kargs[] = {&args};
   return sampled ? cudaLaunchCooperativeKernel(reinterpret_cast<void*>(verify_kernel<true>), grid, kVThreads, kargs, 0,
                                                stream)

@@ -284,8 +284,8 @@ int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* 
  *   accept_len  device int32 [B];  out_tok device int32 [B, L+1]
  * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0.
  * L <= 64, V <= 10,485,760 (DFLASH2_ERR_UNSUPPORTED beyond).
- * The call keeps per-row scratch in the handle (1 MiB from dflash2_create, about
- * 100 bytes per target row).  A call that needs more allocates a larger buffer,
+ * The call keeps per-row scratch in the handle (1 MiB from dflash2_create;
+ * 12 bytes per target row, plus 16 bytes per 4096 vocabulary ids at T > 0).  A call that needs more allocates a larger buffer,
  * after synchronising the device; under stream capture it cannot, and returns
  * DFLASH2_ERR_WORKSPACE instead, so make one call of the largest B * (L+1)
  * before capturing.  Calls on one handle must not overlap on the GPU.

@@ -99,6 +99,30 @@ def test_sampled_verify_is_lossless_on_gpu(handle):
     assert stats.chisquare(obs, exp).pvalue > 1e-4
 
 
+def test_greedy_verify_nan_and_ties(handle):
+    """Arg-max order of the pages' greedy rule as the oracle reads it: NaN ranks
+    below -inf (an all-NaN row's arg-max is id 0), -0 equals +0, and equal
+    values go to the lowest id, wherever in the row (and in which chunk) they lie."""
+    B, L, V = 6, 4, 9000
+    tok, slot, q, ci = draft(7, B, L, V, 0.0)
+    target = synth.target_planted(8, tok, V, agree=0.85)
+    rng = np.random.default_rng(9)
+    f = lambda x: int(synth.bf16_bits(np.float32([x]))[0])   # noqa: E731
+    target[rng.random(target.shape) < 0.05] = 0x7FC0  # NaN scattered everywhere
+    target[0, 1, :] = 0x7FC0                          # all NaN: arg-max 0
+    target[1, 0, :] = f(-1.0)
+    target[1, 0, 8000] = 0x8000                       # -0 at a later id ...
+    target[1, 0, 50] = f(0.0)                         # ... equals +0 at id 50
+    target[2, 0, :] = f(-2.0)
+    target[2, 0, [100, 8000]] = f(3.0)                # a tie in two chunks: id 100
+    tok[2, 0] = 8000
+    target[3, :, tok[3]] = 0x7FC0                     # the draft's own logit is NaN
+    acc, out = api.verify(handle, bf(target), i32(tok), V=V)
+    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci, V=V)
+    assert oout[0, 1] == 0 and oout[1, 0] == 50 and oout[2, 0] == 100
+    assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
+
+
 def test_greedy_mean_acceptance_closed_form_on_gpu(handle):
     B, L, V, r = 4096, 16, 512, 0.85
     rng = np.random.default_rng(8)
