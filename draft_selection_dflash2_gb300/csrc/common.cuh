@@ -32,6 +32,14 @@ __device__ __forceinline__ int32_t clamp_token(int32_t id, int64_t V, uint32_t* 
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
+// Programmatic dependent launch.  pdl_wait blocks until the grid this one was
+// launched after has completed and its writes are visible (a no-op when the
+// launch did not allow programmatic serialization), so it comes before a
+// kernel's first global access; pdl_launch_dependents lets the next grid in
+// the stream be scheduled (its CTAs run their own prologue and then wait).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -307,13 +309,14 @@ cudaError_t launch_splitk_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, c
   cfg.blockDim = dim3(kSkThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = sh.ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, splitk_gemm_kernel<Epi>, tmA, tmB, sh, p, err);
 }
 

@@ -14,6 +14,15 @@ constexpr int kMaxDevices = 64;
 
 // Kernel attributes are per device: these set one for the current device the
 // first time a launch there needs it.  One record per kernel (Fn) and device.
+// A launch attribute that lets the kernel start while the previous kernel in
+// the stream finishes; the kernel calls pdl_wait before its first global access.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a = {};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 template <auto Fn>
 cudaError_t set_smem_limit(size_t bytes) {
   static std::mutex mu;

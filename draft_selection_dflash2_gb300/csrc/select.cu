@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(256) pair_kernel(const int32_t* __restrict__ c
                                                    const uint16_t* __restrict__ Bt, int64_t L,
                                                    int64_t V, float* __restrict__ S,
                                                    uint32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ __align__(16) float G[kTopK][kEmbed];    // A[pred_i] (.) H_t
   __shared__ __align__(16) float Bc[kTopK][kEmbed];   // B[cand_j]
   __shared__ int32_t pred[kTopK], cur[kTopK];
@@ -144,9 +146,14 @@ cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
                                const int32_t* last_verified, const float* gate, const uint16_t* A,
                                const uint16_t* Bt, int64_t B, int64_t L, int64_t V, float* S,
                                uint32_t* err, cudaStream_t stream) {
-  pair_kernel<<<static_cast<unsigned>(B * L), 256, 0, stream>>>(cand_idx, cand_val, last_verified, gate,
-                                                                A, Bt, L, V, S, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B * L), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pair_kernel, cand_idx, cand_val, last_verified, gate, A, Bt, L, V, S, err);
 }
 
 }  // namespace dflash2

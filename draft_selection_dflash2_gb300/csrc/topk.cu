@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
                                                           float* __restrict__ vals,
                                                           int32_t* __restrict__ idx) {
   __shared__ TopkSmem s;
+  pdl_wait();
+  pdl_launch_dependents();
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
   const unsigned nrank = cluster.num_blocks();
@@ -320,13 +322,14 @@ cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk16_kernel, logits, V, ld, seg_len, vals, idx);
 }
 

@@ -475,6 +475,8 @@ __device__ void grid_barrier(unsigned* count, volatile unsigned* gen, volatile u
 // ---------------------------------------------------------------------------
 __global__ void verify_init_kernel(int32_t* first_reject, uint32_t* counters, unsigned long long* keys, unsigned* bar,
                                    int64_t B, int64_t L) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t rows = B * (L + 1);
   if (i < B) first_reject[i] = static_cast<int32_t>(L);
@@ -576,6 +578,7 @@ template <bool kSampled>
 __global__ void __launch_bounds__(kVThreads, kSampled ? kVCtasPerSmSampled : kVCtasPerSm)
     verify_kernel(const VerifyArgs a) {
   __shared__ VerifySmem s;
+  pdl_launch_dependents();   // launched in full order after its init kernel; lets the next kernel prepare
   const int64_t B = a.B, L = a.L, V = a.V;
   const int nch = verify_chunks(V);
   const int64_t cs = verify_chunk_ids(V);
@@ -782,8 +785,19 @@ cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* dra
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   unsigned* bar = reinterpret_cast<unsigned*>(sc);
   const unsigned init_grid = static_cast<unsigned>((rows + 255) / 256);
-  verify_init_kernel<<<init_grid, 256, 0, stream>>>(accept_len, reinterpret_cast<uint32_t*>(sc + lay.counters),
-                                                   reinterpret_cast<unsigned long long*>(sc + lay.keys), bar, B, L);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(init_grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_init_kernel, accept_len,
+                                             reinterpret_cast<uint32_t*>(sc + lay.counters),
+                                             reinterpret_cast<unsigned long long*>(sc + lay.keys), bar, B, L);
+    if (e != cudaSuccess) return e;
+  }
   // the co-resident grid, per device and variant
   static std::mutex mu;
   static int grid_cache[kMaxDevices][2] = {};

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
                 float* __restrict__ draft_q, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) float wsm[];
   __shared__ uint64_t bars[kWalkWarps];
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t b = static_cast<int64_t>(blockIdx.x) * kWalkWarps + warp;
   if (b >= B) return;
@@ -157,9 +159,16 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>((B + kWalkWarps - 1) / kWalkWarps);
-  walk_kernel<<<grid, kWalkWarps * 32, smem, stream>>>(S, cand_idx, B, L, temperature,
-                                                       seed, offset, draft_tok, draft_slot, draft_q, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kWalkWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, walk_kernel, S, cand_idx, B, L, temperature, seed, offset, draft_tok, draft_slot,
+                            draft_q, err);
 }
 
 }  // namespace dflash2
