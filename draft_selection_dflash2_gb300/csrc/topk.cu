@@ -2,7 +2,10 @@
 // Parallel", "A Lightweight Path Selector": keep the top 16 candidates of the
 // drafter's own logits at every block position).
 //
-// Design (HBM-bound stream, 2 bytes per logit):
+// Two forms.  Segments of up to kHistSegMax logits (rows up to 393,216 per
+// CTA, longer ones split over a larger cluster first) take the group-maximum
+// form below (topk16_hist_kernel); longer segments take the running-threshold
+// stream (topk16_kernel):
 //   * A row is split into `S` contiguous segments, one per CTA of an S-CTA
 //     thread-block cluster (S = 1 when there are enough rows to fill the GPU).
 //   * The eight warps of a CTA stream the segment in 512-logit blocks (one
@@ -296,6 +299,195 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
   cluster.sync();
 }
 
+// ---------------------------------------------------------------------------
+// Group-maximum form (segments up to kHistSegMax logits)
+// ---------------------------------------------------------------------------
+// A thread's 8 vectors of one CTA iteration (64 logits) form a group.  The
+// stream keeps only each group's maximum (in shared memory), so a lane's
+// vector is dead once its maximum is taken and its next load is issued at
+// once: the stream runs at close to a plain copy's read rate.  Then
+// T = the 16th largest of the 256 threads' maxima: those are 16 distinct
+// logits >= T, so no logit below T is in the segment's top-16, and every
+// logit of the top-16 lies in a group whose maximum reaches T.  Only those
+// groups (about 16 of a row's 2,400) are read again, by the thread that
+// streamed them (from L2, as a rule), their logits >= T keyed exactly and
+// folded into the warp lists; the segment's few trailing logits (V % 8) are
+// keyed directly.  Rows of ties (every group reaching T) stay exact: the
+// folds take any number of keys.
+constexpr int kHistIters = 24;                                        // CTA iterations a segment may take
+constexpr int64_t kHistSegMax = static_cast<int64_t>(kHistIters) * kThreads * kUnroll * 8;
+
+struct HistSmem {
+  uint32_t hist[kHistIters][kThreads];   // 0: no data; else bf16 order of the group maximum + 1
+  uint64_t cand[kWarps][kWarpCap];
+  uint64_t warp_top[kWarps][kTopK];
+  uint64_t top[kTopK];
+  unsigned long long gthr;
+  uint64_t tkey;                         // the 16th largest thread-maximum key
+  int wcount[kWarps];
+};
+
+__device__ __forceinline__ uint32_t max2_bits(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 m = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&m);
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const uint16_t* __restrict__ logits,
+                                                               int64_t V, int64_t ld, int64_t seg_len,
+                                                               float* __restrict__ vals,
+                                                               int32_t* __restrict__ idx) {
+  __shared__ HistSmem s;
+  pdl_wait();
+  pdl_launch_dependents();
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const unsigned nrank = cluster.num_blocks();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.y;
+
+  const int64_t seg_begin = static_cast<int64_t>(rank) * seg_len;
+  const int64_t seg_end = seg_begin + seg_len < V ? seg_begin + seg_len : V;
+  const int64_t n_elems = seg_end > seg_begin ? seg_end - seg_begin : 0;
+  const int64_t n_vecs = n_elems >> 3;                 // whole 16-byte vectors
+  const uint16_t* seg = logits + row * ld + seg_begin;
+  constexpr int64_t stride = kThreads;                 // vectors between a thread's vectors in an iteration
+  constexpr int64_t per_iter = stride * kUnroll;       // vectors per CTA iteration
+  const int iters = static_cast<int>((n_vecs + per_iter - 1) / per_iter);
+
+  if (tid < kWarps) s.wcount[tid] = 0;
+  if (tid == 0) s.gthr = 0ull;
+
+  // ---- stream: group maxima; a lane reloads each vector as soon as it is reduced
+  const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);   // never a maximum
+  uint4 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t vi = u * stride + tid;
+    v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : nan4;
+  }
+  uint32_t lane_max = 0u;   // the largest of this thread's group entries
+  for (int it = 0; it < iters; ++it) {
+    uint32_t w2[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) w2[u] = max2_bits(max2_bits(v[u].x, v[u].y), max2_bits(v[u].z, v[u].w));
+    const int64_t nb = static_cast<int64_t>(it + 1) * per_iter;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t vi = nb + u * stride + tid;
+      v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : nan4;
+    }
+    const uint32_t m2 = max2_bits(max2_bits(max2_bits(w2[0], w2[1]), max2_bits(w2[2], w2[3])),
+                                  max2_bits(max2_bits(w2[4], w2[5]), max2_bits(w2[6], w2[7])));
+    const __nv_bfloat162 mb = *reinterpret_cast<const __nv_bfloat162*>(&m2);
+    const uint32_t gm = __bfloat16_as_ushort(__hmax(__low2bfloat16(mb), __high2bfloat16(mb)));
+    const bool has = static_cast<int64_t>(it) * per_iter + tid < n_vecs;
+    const uint32_t h = has ? bf16_order(gm) + 1u : 0u;
+    s.hist[it][tid] = h;
+    lane_max = h > lane_max ? h : lane_max;
+  }
+
+  // ---- T: the 16th largest thread maximum (the maxima of 16 threads are 16
+  // distinct logits, so T bounds the segment's 16th best from below)
+  {
+    const uint64_t key = lane_max ? (static_cast<uint64_t>(lane_max) << 32) | static_cast<uint32_t>(~tid) : 0ull;
+    const uint64_t sorted = warp_sort_desc(key, lane);
+    if (lane < kTopK) s.warp_top[warp][lane] = sorted;
+    __syncthreads();   // also publishes the group entries
+    if (warp == 0) {
+      uint64_t a2 = 0ull;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ww += 2) {
+        const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
+        a2 = warp_merge_top16(a2, x, lane);
+      }
+      if (lane == kTopK - 1) s.tkey = a2;
+    }
+    __syncthreads();
+  }
+  // fewer than 16 threads with data: every group with data
+  const uint32_t T = static_cast<uint32_t>(s.tkey >> 32) > 1u ? static_cast<uint32_t>(s.tkey >> 32) : 1u;
+  const uint32_t t_ord = T - 1u;                      // logits of order >= t_ord qualify
+  const uint32_t tb = t_ord ? bf16_from_order(t_ord) : 0u;
+  const __nv_bfloat162 t2 = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(tb)),
+                                               __ushort_as_bfloat16(static_cast<unsigned short>(tb)));
+
+  // ---- the groups that reach T, read again and keyed exactly; each thread
+  // fetches its own, so a warp's first round covers the usual single group
+  WarpSel w{0ull, 0ull};
+  uint64_t* cand = s.cand[warp];
+  int* wcount = &s.wcount[warp];
+  auto next_sel = [&](int from) {
+    int it = from;
+    if (lane_max >= T)
+      while (it < iters && s.hist[it][tid] < T) ++it;
+    else
+      it = iters;
+    return it;
+  };
+  int it = next_sel(0);
+  while (__ballot_sync(0xFFFFFFFFu, it < iters) != 0u) {
+    const bool sel = it < iters;
+    const int64_t b0 = static_cast<int64_t>(sel ? it : 0) * per_iter + tid;
+    uint4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) x[u] = sel && b0 + u * stride < n_vecs ? ldg_stream(seg + (b0 + u * stride) * 8) : nan4;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (sel && b0 + u * stride < n_vecs) {
+        const uint32_t id0 = static_cast<uint32_t>(seg_begin + (b0 + u * stride) * 8);
+        uint32_t em = t_ord == 0u ? 0xFFu : elem_reach_mask(x[u], t2);
+        while (em) {
+          const int k = __ffs(em) - 1;
+          em &= em - 1u;
+          const uint64_t key = make_key(lane_elem(x[u], k), id0 + k);
+          if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
+        }
+      }
+      __syncwarp();
+      if (*reinterpret_cast<volatile int*>(wcount) > kFoldAt) fold_warp(w, cand, wcount, &s.gthr, lane);
+    }
+    it = sel ? next_sel(it + 1) : iters;
+  }
+  if (warp == 0) {
+    const int64_t tail = n_elems - n_vecs * 8;
+    if (lane < tail) {
+      const int64_t e = n_vecs * 8 + lane;
+      const uint64_t key = make_key(seg[e], static_cast<uint32_t>(seg_begin + e));
+      if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
+    }
+  }
+  fold_warp(w, cand, wcount, &s.gthr, lane);
+  if (lane < kTopK) s.warp_top[warp][lane] = w.top;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t acc = 0ull;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ww += 2) {
+      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
+      acc = warp_merge_top16(acc, x, lane);
+    }
+    if (lane < kTopK) s.top[lane] = acc;
+  }
+  // the cluster's lists meet in distributed shared memory
+  cluster.sync();
+  if (rank == 0 && warp == 0) {
+    uint64_t acc = lane < kTopK ? s.top[lane] : 0ull;
+    for (unsigned r = 1; r < nrank; r += 2) {
+      uint64_t x = 0ull;
+      const unsigned src = lane < kTopK ? r : r + 1;
+      if (src < nrank) {
+        const uint64_t* remote = cluster.map_shared_rank(s.top, src);
+        x = remote[lane & (kTopK - 1)];
+      }
+      acc = warp_merge_top16(acc, x, lane);
+    }
+    if (lane < kTopK) {
+      vals[row * kTopK + lane] = key_value(acc);
+      idx[row * kTopK + lane] = key_id(acc);
+    }
+  }
+  cluster.sync();
+}
 }  // namespace
 
 int topk_cluster_size(int64_t rows, int64_t V, int num_sms) {
@@ -310,13 +502,23 @@ int topk_cluster_size(int64_t rows, int64_t V, int num_sms) {
 cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, float* vals,
                         int32_t* idx, uint32_t* err, int num_sms, cudaStream_t stream) {
   (void)err;
+  auto seg_of = [&](int S) {
+    const int64_t l = (V + S - 1) / S;
+    return (l + kSegQuantum - 1) / kSegQuantum * kSegQuantum;
+  };
+  // the group-maximum form while a segment fits its shared-memory history
+  // (splitting a long row over a larger cluster if that makes it fit)
+  const int S0 = topk_cluster_size(rows, V, num_sms);
+  int S = S0;
+  while (S < 16 && seg_of(S) > kHistSegMax) S <<= 1;
+  const bool hist = seg_of(S) <= kHistSegMax;
+  if (!hist) S = S0;
+  const int64_t seg_len = seg_of(S);
   {
-    const cudaError_t e = allow_nonportable_clusters<topk16_kernel>();
+    const cudaError_t e = hist ? allow_nonportable_clusters<topk16_hist_kernel>()
+                               : allow_nonportable_clusters<topk16_kernel>();
     if (e != cudaSuccess) return e;
   }
-  const int S = topk_cluster_size(rows, V, num_sms);
-  int64_t seg_len = (V + S - 1) / S;
-  seg_len = (seg_len + kSegQuantum - 1) / kSegQuantum * kSegQuantum;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, static_cast<unsigned>(rows), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -330,7 +532,8 @@ cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t
   attr[1] = pdl_attribute();
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, topk16_kernel, logits, V, ld, seg_len, vals, idx);
+  return hist ? cudaLaunchKernelEx(&cfg, topk16_hist_kernel, logits, V, ld, seg_len, vals, idx)
+              : cudaLaunchKernelEx(&cfg, topk16_kernel, logits, V, ld, seg_len, vals, idx);
 }
 
 }  // namespace dflash2
