@@ -18,7 +18,7 @@ def check(h, bits, V=None):
     gv, gi = run(h, bits, V)
     ov, oi = oracle.topk(bits, V=V)
     assert np.array_equal(gi, oi), f"idx mismatch in {np.where((gi != oi).any(1))[0][:8]}"
-    assert np.array_equal(gv, ov)
+    assert np.array_equal(gv, ov, equal_nan=True)   # a row of NaN ranks NaN logits (lowest ids first)
     assert h.device_error() == 0
 
 
@@ -72,6 +72,32 @@ def test_topk_adversarial_ascending_rows(handle):
     # every element beats the running threshold: exercises the candidate buffer folds
     base = np.linspace(-8, 8, 40000, dtype=np.float32)
     rows = np.stack([base, base[::-1], np.roll(base, 12345)])
+    check(handle, synth.bf16_bits(rows))
+
+
+def test_topk_edge_rows_on_the_whole_row_path(handle):
+    # enough rows that each CTA takes whole rows (the persistent form with a
+    # ranking warp): ties, signed zeros, NaN runs, all -inf but one, ascending
+    # and descending ramps, planted rows, interleaved so that consecutive rows
+    # of one CTA differ in kind
+    V = 9000
+    rng = np.random.default_rng(6)
+    kinds = []
+    kinds.append(rng.choice(np.array([-1.0, 0.0, 0.5, 2.0], np.float32), size=V))
+    z = np.zeros(V, np.float32)
+    z[::2] = -0.0
+    kinds.append(z)
+    n = rng.standard_normal(V).astype(np.float32)
+    n[100:4000] = np.nan
+    kinds.append(n)
+    f = np.full(V, -np.inf, np.float32)
+    f[8000] = -0.0
+    kinds.append(f)
+    kinds.append(np.linspace(-8, 8, V, dtype=np.float32))
+    kinds.append(np.linspace(8, -8, V, dtype=np.float32))
+    kinds.append(np.full(V, np.nan, np.float32))
+    rows = np.stack([kinds[i % len(kinds)] if i % 3 else rng.standard_normal(V).astype(np.float32)
+                     for i in range(1024)])
     check(handle, synth.bf16_bits(rows))
 
 
