@@ -101,6 +101,15 @@ def test_topk_edge_rows_on_the_whole_row_path(handle):
     check(handle, synth.bf16_bits(rows))
 
 
+@pytest.mark.parametrize("rows,V", [(3, 1_000_000), (2, 6_500_000)])
+def test_topk_long_rows(handle, rows, V):
+    # V = 1M: each row is split over a cluster until a segment fits the group
+    # history (393,216 logits); V = 6.5M exceeds it even over 16 CTAs and
+    # takes the running-threshold stream
+    rng = np.random.default_rng(V + rows)
+    check(handle, synth.logits_planted(rng, rows, V))
+
+
 def test_topk_many_rows_multiple_launches(handle):
     rng = np.random.default_rng(4)
     bits = synth.bf16_bits(rng.standard_normal((70000, 24)).astype(np.float32))
