@@ -166,7 +166,7 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
   int st = launched(dflash2::launch_gate(hs, W_H, b_H, B * L, d, gate, h->err, h->num_sms, s));
   if (st != DFLASH2_OK) return st;
   return launched(dflash2::launch_pair_scores(cand_idx, cand_val, last_verified, gate, A, Bt, B, L, V,
-                                              S, h->err, s));
+                                              S, h->err, h->num_sms, s));
 }
 
 int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,

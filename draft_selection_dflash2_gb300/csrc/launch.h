@@ -62,7 +62,7 @@ cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
                                const int32_t* last_verified, const float* gate, const uint16_t* A,
                                const uint16_t* Bt, int64_t B, int64_t L, int64_t V, float* S,
-                               uint32_t* err, cudaStream_t stream);
+                               uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,

@@ -6,10 +6,12 @@
 //                  the tensor cores (tcgen05 + TMA, fp32 in TMEM, K split over a
 //                  cluster and reduced in distributed shared memory), sigmoid
 //                  fused in the epilogue.
-// pair_kernel      one CTA per block position (b, t): gathers the 16 predecessor
-//                  rows of A and the 16 candidate rows of B (512 B each) with
-//                  16-byte loads, forms G = A_pred (.) H_t in fp32 shared memory,
-//                  and computes the 16 x 16 x 256 products (pair_math.cuh).
+// pair_kernel      persistent, block positions strided over the CTAs: for each
+//                  (b, t) gathers the 16 predecessor rows of A and the 16
+//                  candidate rows of B (512 B each) with 16-byte loads, forms
+//                  G = A_pred (.) H_t in fp32 shared memory and computes the
+//                  16 x 16 x 256 products (pair_math.cuh); the next position's
+//                  rows are gathered while the products run.
 #include "common.cuh"
 #include "gemm_splitk.cuh"
 #include "launch.h"
@@ -64,60 +66,101 @@ struct GateEpi {
 // ---------------------------------------------------------------------------
 // pair scores
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) pair_kernel(const int32_t* __restrict__ cand_idx,
-                                                   const float* __restrict__ cand_val,
-                                                   const int32_t* __restrict__ last_verified,
-                                                   const float* __restrict__ gate,
-                                                   const uint16_t* __restrict__ A,
-                                                   const uint16_t* __restrict__ Bt, int64_t L,
-                                                   int64_t V, float* __restrict__ S,
-                                                   uint32_t* __restrict__ err) {
-  pdl_wait();
-  pdl_launch_dependents();
-  __shared__ __align__(16) float G[kTopK][kEmbed];    // A[pred_i] (.) H_t
-  __shared__ __align__(16) float Bc[kTopK][kEmbed];   // B[cand_j]
-  __shared__ int32_t pred[kTopK], cur[kTopK];
-  const int tid = threadIdx.x;
-  const int64_t pos = blockIdx.x;              // b * L + t
-  const int64_t b = pos / L, t = pos % L;
-  if (tid < kTopK) {
-    const int32_t p = (t == 0) ? last_verified[b] : cand_idx[(pos - 1) * kTopK + tid];
-    pred[tid] = clamp_token(p, V, err);
-    cur[tid] = clamp_token(cand_idx[pos * kTopK + tid], V, err);
-  }
-  __syncthreads();
-  // 32 rows x 32 16-byte chunks = 1024 loads over 256 threads
-  const float* Ht = gate + pos * kEmbed;
+constexpr int kPairCtasPerSm = 3;
+
+// One position's gathered operands, in registers: thread tid's items are rows
+// tid / 32 + 8 it (it = 0, 1: A rows; 2, 3: B rows), 16-byte chunk tid % 32,
+// plus the H_t chunk the A items are scaled by.
+struct PairStage {
+  uint4 raw[4];
+  float4 h0, h1;
+};
+
+__device__ __forceinline__ void pair_issue(PairStage& st, const int32_t* ids, const uint16_t* __restrict__ A,
+                                           const uint16_t* __restrict__ Bt, const float* __restrict__ gate,
+                                           int64_t pos, int tid) {
+  const int ch = tid & 31;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int e = tid + it * 256;
-    const int row = e >> 5, ch = e & 31;       // rows 0..15: A, 16..31: B
-    const bool isA = row < kTopK;
-    const int r16 = row & (kTopK - 1);
-    const uint16_t* src = isA ? A + static_cast<int64_t>(pred[r16]) * kEmbed
-                              : Bt + static_cast<int64_t>(cur[r16]) * kEmbed;
-    const uint4 v = *reinterpret_cast<const uint4*>(src + ch * 8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int row = (tid >> 5) + 8 * it;   // 0..15: A (predecessors), 16..31: B (candidates)
+    const uint16_t* src = row < kTopK ? A + static_cast<int64_t>(ids[row]) * kEmbed
+                                      : Bt + static_cast<int64_t>(ids[row]) * kEmbed;
+    st.raw[it] = *reinterpret_cast<const uint4*>(src + ch * 8);
+  }
+  const float* Ht = gate + pos * kEmbed + ch * 8;
+  st.h0 = *reinterpret_cast<const float4*>(Ht);
+  st.h1 = *reinterpret_cast<const float4*>(Ht + 4);
+}
+
+// G = A_pred (.) H_t and Bc = B_cand in fp32 shared memory.
+__device__ __forceinline__ void pair_store(const PairStage& st, float (*G)[kEmbed], float (*Bc)[kEmbed], int tid) {
+  const int ch = tid & 31;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int row = (tid >> 5) + 8 * it;
+    const uint32_t w[4] = {st.raw[it].x, st.raw[it].y, st.raw[it].z, st.raw[it].w};
     float f[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       f[2 * q] = bf16_bits_to_float(w[q] & 0xFFFFu);
       f[2 * q + 1] = bf16_bits_to_float(w[q] >> 16);
     }
-    if (isA) {
-      const float4 h0 = *reinterpret_cast<const float4*>(Ht + ch * 8);
-      const float4 h1 = *reinterpret_cast<const float4*>(Ht + ch * 8 + 4);
-      f[0] *= h0.x; f[1] *= h0.y; f[2] *= h0.z; f[3] *= h0.w;
-      f[4] *= h1.x; f[5] *= h1.y; f[6] *= h1.z; f[7] *= h1.w;
-      *reinterpret_cast<float4*>(&G[r16][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(&G[r16][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+    if (row < kTopK) {
+      f[0] *= st.h0.x; f[1] *= st.h0.y; f[2] *= st.h0.z; f[3] *= st.h0.w;
+      f[4] *= st.h1.x; f[5] *= st.h1.y; f[6] *= st.h1.z; f[7] *= st.h1.w;
+      *reinterpret_cast<float4*>(&G[row][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(&G[row][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
     } else {
-      *reinterpret_cast<float4*>(&Bc[r16][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(&Bc[r16][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+      *reinterpret_cast<float4*>(&Bc[row - kTopK][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(&Bc[row - kTopK][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
     }
   }
+}
+
+// Persistent: CTA c takes positions c, c + grid, ...  While the products of
+// one position run, the rows of the next are in flight in registers and the
+// ids of the one after that are loading.
+__global__ void __launch_bounds__(256, kPairCtasPerSm) pair_kernel(const int32_t* __restrict__ cand_idx,
+                                                                   const float* __restrict__ cand_val,
+                                                                   const int32_t* __restrict__ last_verified,
+                                                                   const float* __restrict__ gate,
+                                                                   const uint16_t* __restrict__ A,
+                                                                   const uint16_t* __restrict__ Bt, int64_t L,
+                                                                   int64_t V, int64_t npos, float* __restrict__ S,
+                                                                   uint32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ __align__(16) float G[kTopK][kEmbed];    // A[pred_i] (.) H_t
+  __shared__ __align__(16) float Bc[kTopK][kEmbed];   // B[cand_j]
+  __shared__ int32_t ids[2][2 * kTopK];               // pred (0..15) and cand (16..31) ids of coming positions
+  const int tid = threadIdx.x;
+  const int64_t stride = gridDim.x;
+  int64_t pos = blockIdx.x;
+  if (pos >= npos) return;
+  // thread q < 32: predecessor (q < 16) or candidate (q >= 16) id q of position p
+  auto load_id = [&](int64_t p) -> int32_t {
+    const int64_t b = p / L, t = p % L;
+    const int32_t v = tid < kTopK ? (t == 0 ? last_verified[b] : cand_idx[(p - 1) * kTopK + tid])
+                                  : cand_idx[p * kTopK + tid - kTopK];
+    return clamp_token(v, V, err);
+  };
+  if (tid < 2 * kTopK) ids[0][tid] = load_id(pos);
+  int32_t next_id = tid < 2 * kTopK && pos + stride < npos ? load_id(pos + stride) : 0;
   __syncthreads();
-  pair_products(G, Bc, cand_val, S, pos, tid);
+  PairStage st;
+  pair_issue(st, ids[0], A, Bt, gate, pos, tid);
+  int buf = 0;
+  for (; pos < npos; pos += stride) {
+    const int64_t pn = pos + stride;
+    pair_store(st, G, Bc, tid);
+    if (tid < 2 * kTopK) ids[buf ^ 1][tid] = next_id;
+    next_id = tid < 2 * kTopK && pn + stride < npos ? load_id(pn + stride) : 0;
+    __syncthreads();   // G, Bc and the next position's ids are in place
+    if (pn < npos) pair_issue(st, ids[buf ^ 1], A, Bt, gate, pn, tid);
+    pair_products(G, Bc, cand_val, S, pos, tid);
+    __syncthreads();   // G and Bc are free again
+    buf ^= 1;
+  }
 }
 
 }  // namespace
@@ -145,15 +188,17 @@ cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
                                const int32_t* last_verified, const float* gate, const uint16_t* A,
                                const uint16_t* Bt, int64_t B, int64_t L, int64_t V, float* S,
-                               uint32_t* err, cudaStream_t stream) {
+                               uint32_t* err, int num_sms, cudaStream_t stream) {
+  const int64_t npos = B * L;
+  const int64_t slots = static_cast<int64_t>(kPairCtasPerSm) * num_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(B * L), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(npos < slots ? npos : slots), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pair_kernel, cand_idx, cand_val, last_verified, gate, A, Bt, L, V, S, err);
+  return cudaLaunchKernelEx(&cfg, pair_kernel, cand_idx, cand_val, last_verified, gate, A, Bt, L, V, npos, S, err);
 }
 
 }  // namespace dflash2
