@@ -109,6 +109,27 @@ struct WarpSel {
   uint64_t thr;
 };
 
+// top: a descending top-16 in lanes 0..15 (0 in lanes 16..31); x: a bitonic
+// sequence, a descending 16-list in lanes 0..15 and another in reverse
+// (ascending) in lanes 16..31.  Returns the top-16 of the three lists: five
+// bitonic merge stages sort x (two sorted lists need no full sort), five more
+// merge it with top.  Whole warp.
+__device__ __forceinline__ uint64_t merge_sorted_pair(uint64_t top, uint64_t x, int lane) {
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+    x = ((lane & j) == 0) ? kmax(x, o) : kmin(x, o);
+  }
+  const uint64_t xr = __shfl_sync(0xFFFFFFFFu, x, 31 - lane);
+  uint64_t c = kmax(top, xr);
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, c, j);
+    c = ((lane & j) == 0) ? kmax(c, o) : kmin(c, o);
+  }
+  return lane < kTopK ? c : 0ull;
+}
+
 // Rare path, kept out of line so the streaming loop stays small: appends the
 // keys of one lane's vector (first id id0) that beat `thr` to the warp buffer.
 __device__ __noinline__ void append_vector(uint64_t* cand, int* wcount, uint4 v, uint32_t id0, uint64_t thr) {
@@ -187,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
       uint64_t acc = 0ull;
 #pragma unroll
       for (int ww = 0; ww < kWarps; ww += 2) {
-        const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
-        acc = warp_merge_top16(acc, x, lane);
+        const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][31 - lane];
+        acc = merge_sorted_pair(acc, x, lane);
       }
       if (lane == kTopK - 1) s.gthr = acc;
     }
@@ -272,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
     uint64_t acc = 0ull;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ww += 2) {
-      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
-      acc = warp_merge_top16(acc, x, lane);
+      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][31 - lane];
+      acc = merge_sorted_pair(acc, x, lane);
     }
     if (lane < kTopK) s.top[lane] = acc;
   }
@@ -287,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
       const unsigned src = lane < kTopK ? r : r + 1;
       if (src < nrank) {
         const uint64_t* remote = cluster.map_shared_rank(s.top, src);
-        x = remote[lane & (kTopK - 1)];
+        x = remote[lane < kTopK ? lane : 31 - lane];
       }
-      acc = warp_merge_top16(acc, x, lane);
+      acc = merge_sorted_pair(acc, x, lane);
     }
     if (lane < kTopK) {
       vals[row * kTopK + lane] = key_value(acc);
@@ -397,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
       uint64_t a2 = 0ull;
 #pragma unroll
       for (int ww = 0; ww < kWarps; ww += 2) {
-        const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
-        a2 = warp_merge_top16(a2, x, lane);
+        const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][31 - lane];
+        a2 = merge_sorted_pair(a2, x, lane);
       }
       if (lane == kTopK - 1) s.tkey = a2;
     }
@@ -463,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
     uint64_t acc = 0ull;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ww += 2) {
-      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][lane - kTopK];
-      acc = warp_merge_top16(acc, x, lane);
+      const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][31 - lane];
+      acc = merge_sorted_pair(acc, x, lane);
     }
     if (lane < kTopK) s.top[lane] = acc;
   }
@@ -477,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
       const unsigned src = lane < kTopK ? r : r + 1;
       if (src < nrank) {
         const uint64_t* remote = cluster.map_shared_rank(s.top, src);
-        x = remote[lane & (kTopK - 1)];
+        x = remote[lane < kTopK ? lane : 31 - lane];
       }
-      acc = warp_merge_top16(acc, x, lane);
+      acc = merge_sorted_pair(acc, x, lane);
     }
     if (lane < kTopK) {
       vals[row * kTopK + lane] = key_value(acc);
