@@ -346,6 +346,7 @@ struct HistSmem {
   unsigned long long gthr;
   uint64_t tkey;                         // the 16th largest thread-maximum key
   int wcount[kWarps];
+  int wfold[kWarps];                     // the warp folded its buffer during the re-read
 };
 
 __device__ __forceinline__ uint32_t max2_bits(uint32_t a, uint32_t b) {
@@ -477,15 +478,38 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
       if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
     }
   }
-  fold_warp(w, cand, wcount, &s.gthr, lane);
+  // Warp 0 merges the lists of the warps that folded (usually none) and then
+  // every key still buffered, 32 at a time over all warps' buffers (usually
+  // one round), instead of a fold per warp and a merge of eight lists.
+  const bool folded = __any_sync(0xFFFFFFFFu, w.top != 0ull);
   if (lane < kTopK) s.warp_top[warp][lane] = w.top;
+  if (lane == 0) s.wfold[warp] = folded ? 1 : 0;
   __syncthreads();
   if (warp == 0) {
     uint64_t acc = 0ull;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ww += 2) {
+      if (!(s.wfold[ww] | s.wfold[ww + 1])) continue;
       const uint64_t x = (lane < kTopK) ? s.warp_top[ww][lane] : s.warp_top[ww + 1][31 - lane];
       acc = merge_sorted_pair(acc, x, lane);
+    }
+    int cnt[kWarps], total = 0;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      cnt[ww] = s.wcount[ww];
+      total += cnt[ww];
+    }
+    for (int base = 0; base < total; base += 32) {
+      int i = base + lane;
+      uint64_t key = 0ull;
+      if (i < total) {
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) {
+          if (i >= 0 && i < cnt[ww]) key = s.cand[ww][i];
+          i -= cnt[ww];
+        }
+      }
+      acc = warp_merge_top16(acc, key, lane);
     }
     if (lane < kTopK) s.top[lane] = acc;
   }
