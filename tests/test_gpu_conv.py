@@ -19,8 +19,9 @@ def run(h, c, hs=None, y_fp32=True):
 
 @pytest.mark.parametrize("B,L,d,bias", [(1, 16, 2560, False), (2, 5, 192, True), (8, 16, 5120, False),
                                         (3, 64, 512, True), (1, 1, 64, False), (16, 16, 2560, True),
-                                        (24, 16, 5120, False)])
+                                        (24, 16, 5120, False), (128, 16, 5120, True)])
 def test_conv_fp32_matches_oracle(handle, B, L, d, bias):
+    # (128, 16, 5120): the benchmark's shape, 32 tiles with the K loop split 4 ways
     c = synth.conv_inputs(B * 13 + L, B, L, d, with_bias=bias)
     y = run(handle, c)
     oy = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c, b_c=c.b_c)

@@ -76,6 +76,31 @@ def test_sampled_verify_matches_oracle(handle, B, L, V, plant, T):
     assert handle.device_error() == 0
 
 
+def test_verify_full_size_both_temperatures(handle):
+    # the benchmark's shape and launch configuration: B=128, L=16, V=151936
+    # (661 MB of target logits), where the grid's warps equal sequences x chunks
+    B, L, V = 128, 16, 151936
+    tok, slot, q, ci = draft(12, B, L, V, 1.0)
+    target = synth.target_planted(13, tok, V, agree=0.85, plant=8.0)
+    tg = bf(target)
+    acc, out = api.verify(handle, tg, i32(tok), V=V)
+    oacc, oout, _ = oracle.verify(target, tok, slot, q, ci, V=V)
+    assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
+    assert oacc.mean() > 4.0   # most sequences reach deep positions: the tail of the pass is covered
+    acc, out = api.verify(handle, tg, i32(tok), i32(slot), f32(q), i32(ci), temperature=1.0, seed=5, offset=1,
+                          V=V)
+    oacc, oout, margin = oracle.verify(target, tok, slot, q, ci, temperature=1.0, seed=5, offset=1, V=V)
+    # with 151936 ids a drawn token's own mass is ~7e-6 of the total, so many draws
+    # land within the draw margin of a neighbour; the accept tests rarely do
+    accept_ok = margin[:, 0] >= ACCEPT_MARGIN
+    assert accept_ok.sum() >= B - 2
+    assert np.array_equal(host(acc)[accept_ok], oacc[accept_ok])
+    ok = ~excused(margin)
+    assert ok.sum() >= B // 4
+    assert np.array_equal(host(out)[ok], oout[ok])
+    assert handle.device_error() == 0
+
+
 def test_sampled_verify_is_lossless_on_gpu(handle):
     V, L, n, T = 64, 2, 20000, 1.0
     rng = np.random.default_rng(31)
