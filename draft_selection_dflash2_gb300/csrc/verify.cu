@@ -164,27 +164,47 @@ __device__ __forceinline__ void load_batch(uint4 (&v)[U], const uint4* rv, int b
 }
 
 // Largest key of the chunk.  Each lane keeps its best vector maximum, the
-// first vector holding it (a strict > in increasing vector order keeps the
-// first; a lane's first vector starts as best even if all NaN) and that
-// vector's data, then names the lowest id with that value; the warp takes the
-// largest key.  0 only for an empty chunk.  v holds the first batch on entry.
+// first vector holding it (a lane's first vector starts as best even if all
+// NaN) and that vector's data, then names the lowest id with that value; the
+// warp takes the largest key.  0 only for an empty chunk.  Per batch the lane
+// first takes the batch maximum (a tree over the vectors' maxima); only a
+// batch that beats the lane's best (the first, as a rule, then rarely) looks
+// for its first vector holding that maximum.  v holds the first batch on entry.
 template <int U>
-__device__ __forceinline__ uint64_t warp_chunk_argmax(uint4 (&v)[U], const uint4* rv, int64_t v0, int64_t v1, const uint16_t* row,
-                                      int lane) {
+__device__ __forceinline__ uint64_t warp_chunk_argmax(uint4 (&v)[U], const uint4* rv, int64_t v0, int64_t v1,
+                                                      const uint16_t* row, int lane) {
   const int nvec = static_cast<int>((v1 - v0) >> 3);
   uint32_t best = 0u;
   int best_i = -1;
   uint4 bestv = make_uint4(0, 0, 0, 0);
   for (int base = 0;;) {
+    uint32_t vm[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + lane + 32 * u;
-      if (i < nvec) {
-        const uint32_t vo = bf16_order(vec_max_bits(v[u]));
-        const bool better = best_i < 0 || vo > best;
-        best = better ? vo : best;
-        best_i = better ? i : best_i;
-        bestv = better ? v[u] : bestv;
+    for (int u = 0; u < U; ++u) vm[u] = base + lane + 32 * u < nvec ? vec_max_bits(v[u]) : 0x7FC0u;   // NaN: never a maximum
+    uint32_t bm = vm[0];
+#pragma unroll
+    for (int u = 1; u < U; ++u) {
+      const __nv_bfloat16 m = __hmax(__ushort_as_bfloat16(static_cast<unsigned short>(bm)),
+                                     __ushort_as_bfloat16(static_cast<unsigned short>(vm[u])));
+      bm = __bfloat16_as_ushort(m);
+    }
+    if (base + lane < nvec) {
+      const uint32_t bo = bf16_order(bm);
+      if (best_i < 0 || bo > best) {
+        // the batch's first vector holding its maximum (its first vector if all NaN)
+        const float bf = bf16_bits_to_float(bm);
+        int pick = 0;
+        uint4 pv = v[0];
+#pragma unroll
+        for (int u = U - 1; u >= 0; --u) {
+          if (base + lane + 32 * u < nvec && bf16_bits_to_float(vm[u]) == bf) {
+            pick = u;
+            pv = v[u];
+          }
+        }
+        best = bo;
+        best_i = base + lane + 32 * pick;
+        bestv = pv;
       }
     }
     base += 32 * U;
