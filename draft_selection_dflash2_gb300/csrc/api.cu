@@ -255,8 +255,9 @@ int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const 
   if (!(temperature == temperature)) return DFLASH2_ERR_INVALID_ARG;
   if (B == 0) return DFLASH2_OK;
   const bool sampled = temperature > 0.0f;
-  if (!target || !draft_tok || !accept_len || !out_tok) return DFLASH2_ERR_INVALID_ARG;
-  if (sampled && (!draft_slot || !draft_q || !cand_idx)) return DFLASH2_ERR_INVALID_ARG;
+  // an empty block (L = 0) reads no draft: only the bonus row is decided
+  if (!target || (L > 0 && !draft_tok) || !accept_len || !out_tok) return DFLASH2_ERR_INVALID_ARG;
+  if (sampled && L > 0 && (!draft_slot || !draft_q || !cand_idx)) return DFLASH2_ERR_INVALID_ARG;
   if (!aligned(target, 16) || (ld % 8) != 0 || !aligned(draft_tok, 4) || !aligned(accept_len, 4) ||
       !aligned(out_tok, 4) || (draft_slot && !aligned(draft_slot, 4)) ||
       (draft_q && !aligned(draft_q, 4)) || (cand_idx && !aligned(cand_idx, 4)))

@@ -282,7 +282,8 @@ int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* 
  *   draft_tok, draft_slot  device int32 [B, L];  draft_q device fp32 [B, L, 16]
  *   cand_idx    device int32 [B, L, 16]
  *   accept_len  device int32 [B];  out_tok device int32 [B, L+1]
- * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0.
+ * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0, and every
+ * draft argument may be NULL when L = 0 (only the bonus row is decided).
  * L <= 64, V <= 10,485,760 (DFLASH2_ERR_UNSUPPORTED beyond).
  * The call keeps per-row scratch in the handle (1 MiB from dflash2_create;
  * 12 bytes per target row, plus 16 bytes per 4096 vocabulary ids at T > 0).  A call that needs more allocates a larger buffer,

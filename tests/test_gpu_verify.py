@@ -148,6 +148,22 @@ def test_greedy_verify_nan_and_ties(handle):
     assert np.array_equal(host(acc), oacc) and np.array_equal(host(out), oout)
 
 
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_verify_empty_block(handle, T):
+    # L = 0: no draft, only the bonus row; the draft tensors are empty (null pointers)
+    B, L, V, K = 5, 0, 4099, 16
+    rng = np.random.default_rng(17)
+    target = padded(synth.bf16_bits(rng.standard_normal((B, L + 1, V)).astype(np.float32)), V)
+    tok, slot = np.zeros((B, L), np.int32), np.zeros((B, L), np.int32)
+    q, ci = np.zeros((B, L, K), np.float32), np.zeros((B, L, K), np.int32)
+    acc, out = api.verify(handle, bf(target), i32(tok), i32(slot), f32(q), i32(ci), temperature=T, seed=3, V=V)
+    oacc, oout, margin = oracle.verify(target, tok, slot, q, ci, temperature=T, seed=3, V=V)
+    ok = ~excused(margin)
+    assert ok.sum() >= B - 1
+    assert np.array_equal(host(acc), oacc) and np.array_equal(host(out)[ok], oout[ok])
+    assert handle.device_error() == 0
+
+
 def test_greedy_mean_acceptance_closed_form_on_gpu(handle):
     B, L, V, r = 4096, 16, 512, 0.85
     rng = np.random.default_rng(8)
