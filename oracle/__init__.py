@@ -37,6 +37,8 @@ def _load():
         lib.oracle_uniform24.restype = D
         lib.oracle_exp2_neg.argtypes = [ctypes.c_float]
         lib.oracle_exp2_neg.restype = ctypes.c_float
+        lib.oracle_verify_weights.argtypes = [P, I64, D, P]
+        lib.oracle_verify_weights.restype = U64
         lib.oracle_topk.argtypes = [P, I64, I64, I64, I, P, P, I]
         lib.oracle_topk.restype = None
         lib.oracle_gate.argtypes = [P, P, P, I64, I64, I64, P, I]
@@ -98,6 +100,14 @@ def uniform24(seed, b, t, stream, offset=0):
 def exp2_neg(x: float) -> float:
     """The walk's fp32 2^x (x <= 0): Cody-Waite reduction + degree-7 Taylor polynomial."""
     return float(_load().oracle_exp2_neg(float(x)))
+
+
+def verify_weights(row_bits, temperature):
+    """Reading R21: fixed-point weights of one target row -> (W uint64 [V], Z)."""
+    row = _c(row_bits, np.uint16)
+    W = np.zeros(row.shape[0], np.uint64)
+    Z = _load().oracle_verify_weights(_p(row), row.shape[0], float(temperature), _p(W))
+    return W, int(Z)
 
 
 def topk(logits_bits, k=16, V=None, nthreads=None):
@@ -245,7 +255,8 @@ def verify(target_bits, draft_tok, draft_slot, draft_q, cand_idx, temperature=0.
     """target: uint16 [B, L+1, ld] -> (accept_len [B], out_tok [B, L+1], margin [B, 2]).
 
     margin[:, 0]: smallest relative accept-test margin; margin[:, 1]: smallest
-    draw margin relative to the total mass (both +inf at temperature 0)."""
+    draw margin relative to the total weight (both +inf at temperature 0).  At
+    T > 0 the decisions are taken on reading R21's exact fixed-point weights."""
     tg = _c(target_bits, np.uint16)
     dt = _c(draft_tok, np.int32)
     ds = _c(draft_slot, np.int32)

@@ -22,19 +22,41 @@
 //   R2  context gate H(h_t) = sigmoid(W_H h_t + b_H), one 256-vector per position.
 //   R3  position t = 0 has a single predecessor, the last verified token; the 16
 //       rows of its 16x16 score block are identical.
-//   R4  greedy walk = myopic best successor at every step, lowest slot on ties.
+//   R4  greedy walk = myopic best successor at every step, lowest slot on ties;
+//       a NaN score never beats a number (R1's order: NaN below -inf), so a
+//       row's choice is the lowest slot of its largest non-NaN score (slot 0
+//       if every score is NaN).
 //   R5  sampled walk = softmax(S/T) over the 16 successors of the chosen
 //       predecessor, inverse CDF in slot order with a Philox4x32-10 uniform.
 //       The draw is an integer decided by floating point, so it is taken in
 //       the kernel's precision (fp32) with 2^x evaluated by a named method
 //       (Cody-Waite reduction + degree-7 Taylor polynomial, exp2_neg below):
 //       every step is a correctly rounded IEEE fp32 operation, so any
-//       implementation of the same steps draws the same slot.
+//       implementation of the same steps draws the same slot.  A row with no
+//       positive weight (every score NaN or -inf) takes the greedy choice,
+//       with q one-hot there.
 //   R6  conv correction [c0; c1] = W_c h_t (+ b_c), linear, no activation;
 //       rows [0, d/16) give c0, rows [d/16, 2d/16) give c1; channel ch belongs
 //       to group ch/16; h defaults to the conv input x; no residual.
 //   R7  verification at T > 0 is standard speculative rejection sampling with
 //       proposal q = the walk's per-step 16-slot distribution (zero elsewhere).
+//   R21 the target distribution of R7 in exact fixed point.  Every accept test
+//       and draw is an integer decided by floating point, so both sides take
+//       the weights in one precision and sum them exactly:
+//         c = fp32(log2 e) / T (fp32), M = the row's largest non-NaN logit,
+//         w_v = exp2_neg((l_v - M) * c) (fp32, R5's function),
+//         W_v = floor(w_v * 2^40) (an integer; weights below 2^-40 of the
+//         row's largest count as 0), Z = sum_v W_v (exact in 64 bits for
+//         V < 2^23), p(v) = W_v / Z.
+//       Integer sums do not depend on their order, so any parallel split of a
+//       row gives the same Z and the same prefix sums.  Accept t iff
+//       (u1 * q) * Z < W_x in fp64 (u1 * q is exact; one rounding).  The
+//       residual of a rejection is R_v = max(0, W_v - sum_{j: c_j = v} Q_j) with
+//       Q_j = floor(q_j * Z) (fp64 product, truncated); the draw target is
+//       floor(U * R / 2^24) for the 24-bit Philox integer U and R = sum_v R_v,
+//       and the token is the lowest id whose inclusive prefix of R exceeds it.
+//       If R = 0 the draw uses W; if Z = 0 (no finite logit) the token is the
+//       row's arg-max in R1's order.  The bonus row draws from W the same way.
 //   R8  Philox counter = (b, t | stream << 24, offset_lo, offset_hi),
 //       key = (seed_lo, seed_hi); a uniform is (x0 >> 8) * 2^-24.
 //   R17 exact best-path walk (the pages call pairwise scoring "the simplest
@@ -168,6 +190,43 @@ int64_t clamp_id(int64_t id, int64_t V, int* flag) {
   return id;
 }
 
+// The 24-bit Philox integer behind uniform24 (reading R8): u = U * 2^-24.
+uint64_t uniform24_bits(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, uint64_t offset) {
+  return static_cast<uint64_t>(uniform24(seed, b, t, stream, offset) * 16777216.0);
+}
+
+// Reading R21: floor(w * 2^40) for an fp32 weight w (0 for w <= 0 and NaN).
+// w * 2^40 is exact in double (a 24-bit mantissa scaled by a power of two) and
+// the conversion truncates toward zero.
+uint64_t fixed_weight(float w) {
+  if (!(w > 0.0f)) return 0;
+  return static_cast<uint64_t>(std::ldexp(static_cast<double>(w), 40));
+}
+
+// Reading R21: the fixed-point weights W_v of one target row at inverse
+// temperature c, returning Z = sum_v W_v (exact).  M is the largest non-NaN
+// logit (NaN if there is none, which makes every weight 0).
+uint64_t fixed_row_weights(const uint16_t* row, int64_t V, float c, uint64_t* W) {
+  float M = std::numeric_limits<float>::quiet_NaN();
+  for (int64_t v = 0; v < V; ++v) {
+    const float l = widen_bf16_f(row[v]);
+    if (!std::isnan(l) && (std::isnan(M) || l > M)) M = l;
+  }
+  uint64_t Z = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    const float x = (widen_bf16_f(row[v]) - M) * c;
+    W[v] = fixed_weight(exp2_neg(x));
+    Z += W[v];
+  }
+  return Z;
+}
+
+// floor(U * total / 2^24) exactly, for U < 2^24 (the draw target of reading R21).
+uint64_t scaled_target(uint64_t U, uint64_t total) {
+  const unsigned __int128 p = static_cast<unsigned __int128>(U) * total;
+  return static_cast<uint64_t>(p >> 24);
+}
+
 }  // namespace
 
 extern "C" {
@@ -183,6 +242,14 @@ double oracle_uniform24(uint64_t seed, uint64_t b, uint64_t t, uint32_t stream, 
 }
 
 float oracle_exp2_neg(float x) { return exp2_neg(x); }
+
+// Reading R21's fixed-point weights of one target row (bf16 bits, V ids) at
+// temperature T: W[v] = floor(exp2_neg((l_v - M) * c) * 2^40), c = fp32(log2 e) / T;
+// returns Z = sum_v W[v].
+uint64_t oracle_verify_weights(const uint16_t* row, int64_t V, double temperature, uint64_t* W) {
+  const float c = 1.44269504f / static_cast<float>(temperature);
+  return fixed_row_weights(row, V, c, W);
+}
 
 // ---------------------------------------------------------------------------
 // Stage 1: per-position top-k candidates.
@@ -318,13 +385,15 @@ int oracle_pair_scores_proj(const int32_t* cand_idx, const float* cand_val, cons
 // starting from the last verified token, greedy follows the best successor at
 // each step; sampling draws from the same scores.
 //   row(t) = 0 for t = 0 (all rows are equal there), else slot(t - 1).
-//   temperature <= 0: slot(t) = lowest j maximising S[b, t, row, j] (R4);
+//   temperature <= 0: slot(t) = lowest j maximising S[b, t, row, j] over the
+//                     non-NaN scores (R4; 0 if all are NaN);
 //                     q[b, t, :] = one-hot at slot(t).
-//   temperature  > 0 (R5, all in fp32): c = log2(e) / T,
-//                     w_j = exp2_neg((S_j - max S) * c), Z = w_0 + ... + w_15 summed
-//                     in slot order, u = uniform24(seed, b, t, 0, offset) (exact in
-//                     fp32), slot(t) = smallest j with u * Z < w_0 + ... + w_j;
-//                     q[b, t, j] = w_j / Z.
+//   temperature  > 0 (R5, all in fp32): c = log2(e) / T, m = the greedy slot's
+//                     score, w_j = exp2_neg((S_j - m) * c), Z = w_0 + ... + w_15
+//                     summed in slot order, u = uniform24(seed, b, t, 0, offset)
+//                     (exact in fp32), slot(t) = smallest j with u * Z < w_0 + ... + w_j;
+//                     q[b, t, j] = w_j / Z.  If Z = 0 (every score NaN or -inf),
+//                     slot(t) = the greedy slot and q is one-hot there.
 // S: [B, L, K, K] fp32 (the walk reads scores at the precision they are stored);
 // outputs draft_tok, draft_slot: [B, L]; q: [B, L, K] or null;
 // margin: [B, L] or null -- the decision margin of every step (greedy: best -
@@ -341,9 +410,10 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
       double step_margin = 0.0;
       const int64_t row = (t == 0) ? 0 : prev;
       const float* s = S + ((b * L + t) * K + row) * K;
+      // lowest slot of the largest non-NaN score (R4); slot 0 if all are NaN
       int64_t best = 0;
       for (int64_t j = 1; j < K; ++j)
-        if (s[j] > s[best]) best = j;
+        if (!std::isnan(s[j]) && (std::isnan(s[best]) || s[j] > s[best])) best = j;
       int64_t chosen;
       if (temperature <= 0.0) {
         chosen = best;
@@ -363,25 +433,33 @@ void oracle_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, 
           Z += w[j];
           cdf[j] = Z;
         }
-        const float u = static_cast<float>(uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 0, offset));
-        const float target = u * Z;
-        chosen = -1;
-        for (int64_t j = 0; j < K; ++j)
-          if (target < cdf[j]) {
-            chosen = j;
-            break;
-          }
-        if (chosen < 0)
-          for (int64_t j = K - 1; j >= 0; --j)
-            if (w[j] > 0.0f) {
+        if (!(Z > 0.0f)) {
+          // no positive weight (every score NaN or -inf): the greedy choice (R5)
+          chosen = best;
+          step_margin = std::numeric_limits<double>::infinity();
+          if (q)
+            for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = (j == chosen) ? 1.0f : 0.0f;
+        } else {
+          const float u = static_cast<float>(uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 0, offset));
+          const float target = u * Z;
+          chosen = -1;
+          for (int64_t j = 0; j < K; ++j)
+            if (target < cdf[j]) {
               chosen = j;
               break;
             }
-        double gap = static_cast<double>(cdf[chosen]) - target;
-        if (chosen > 0) gap = std::min(gap, static_cast<double>(target) - cdf[chosen - 1]);
-        step_margin = gap / Z;
-        if (q)
-          for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = w[j] / Z;
+          if (chosen < 0)
+            for (int64_t j = K - 1; j >= 0; --j)
+              if (w[j] > 0.0f) {
+                chosen = j;
+                break;
+              }
+          double gap = static_cast<double>(cdf[chosen]) - target;
+          if (chosen > 0) gap = std::min(gap, static_cast<double>(target) - cdf[chosen - 1]);
+          step_margin = gap / Z;
+          if (q)
+            for (int64_t j = 0; j < K; ++j) q[(b * L + t) * K + j] = w[j] / Z;
+        }
       }
       draft_slot[b * L + t] = static_cast<int32_t>(chosen);
       draft_tok[b * L + t] = cand_idx[(b * L + t) * K + chosen];
@@ -475,20 +553,23 @@ void oracle_gemm_conv2tap(const uint16_t* A, const uint16_t* W, const uint16_t* 
 // temperature <= 0 (greedy): a_t = lowest id maximising target[b, t, :]
 //   (values compared exactly); n = first t < L with draft_tok[b, t] != a_t,
 //   else L; out = draft[0..n-1], a_n; accept_len = n + 1.
-// temperature > 0 (reading R7): for t = 0..L-1 with p_t = softmax(target_t / T)
-//   (double), x = draft_tok[t], q = draft_q[t, draft_slot[t]],
-//   u = uniform24(seed, b, t, 1, offset): accept iff u * q < p_t(x).
-//   On the first rejection at t: draw from the residual r_v = max(0, p_t(v) - q_t(v))
-//   (q_t(v) = draft_q[t, j] where cand_idx[t, j] = v, else 0) by inverse CDF
-//   in id order with u' = uniform24(seed, b, t, 2, offset); accept_len = t + 1.
-//   If all L are accepted: draw the bonus token from p_L the same way with
-//   uniform24(seed, b, L, 2, offset); accept_len = L + 1.
+// temperature > 0 (readings R7 and R21): for t = 0..L-1 with p_t(v) = W_v / Z
+//   (the fixed-point weights of row t), x = draft_tok[t] (W_x = 0 outside
+//   [0, V)), q = draft_q[t, draft_slot[t]] (slot clamped to [0, 16)),
+//   u1 = uniform24(seed, b, t, 1, offset): accept iff (u1 * q) * Z < W_x.
+//   On the first rejection at t: draw from the residual R_v = max(0, W_v -
+//   sum_{j: cand_idx[t, j] = v} Q_j), Q_j = floor(min(q_j, 1) * Z) (q_j = draft_q[t, j],
+//   NaN or negative read as 0), by inverse CDF in id order with the target
+//   floor(U2 * R / 2^24), U2 the 24-bit integer of (b, t, stream 2);
+//   accept_len = t + 1.  If all L are accepted: draw the bonus token from W of
+//   row L the same way with the integer of (b, L, stream 2); accept_len = L + 1.
 // target: [B, L + 1, ld] bf16 (row (b, t) starts at (b * (L + 1) + t) * ld);
 // out_tok: [B, L + 1], -1 after the last emitted token.
 // margin: [B, 2] or null -- T > 0 only (+inf at T = 0, whose decisions are
-// exact): [0] the smallest |u q - p(x)| / p(x) over the accept tests on the
-// path, [1] the smallest distance of a draw's target mass to the CDF boundaries
-// of the drawn token, relative to the total mass.
+// exact): [0] the smallest |u1 q Z - W_x| / W_x over the accept tests on the
+// path, [1] the smallest distance of a draw's target to the bounds of the
+// drawn token's interval, relative to the total.  They say how close a
+// decision came to flipping, for comparisons with a floating-point restatement.
 // ---------------------------------------------------------------------------
 void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                    const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
@@ -516,68 +597,74 @@ void oracle_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
         }
       }
     } else {
-      std::vector<double> p(static_cast<size_t>(V));
-      auto softmax_row = [&](int64_t t) {
-        const uint16_t* row = target + (b * (L + 1) + t) * ld;
-        double m = -std::numeric_limits<double>::infinity();
-        for (int64_t v = 0; v < V; ++v) m = std::max(m, widen_bf16(row[v]));
-        double Z = 0.0;
-        for (int64_t v = 0; v < V; ++v) {
-          p[v] = std::exp((widen_bf16(row[v]) - m) / temperature);
-          Z += p[v];
-        }
-        for (int64_t v = 0; v < V; ++v) p[v] /= Z;
+      const float c = 1.44269504f / static_cast<float>(temperature);
+      std::vector<uint64_t> W(static_cast<size_t>(V)), R(static_cast<size_t>(V)), Qs(static_cast<size_t>(V));
+      std::vector<char> is_cand(static_cast<size_t>(V));
+      auto row_of = [&](int64_t t) { return target + (b * (L + 1) + t) * ld; };
+      // the row's arg-max in R1's order (the token when no weight is positive)
+      auto argmax_row = [&](int64_t t) -> int32_t {
+        const uint16_t* row = row_of(t);
+        int64_t a = 0;
+        for (int64_t v = 1; v < V; ++v)
+          if (ranks_before(widen_bf16(row[v]), v, widen_bf16(row[a]), a)) a = v;
+        return static_cast<int32_t>(a);
       };
-      // Inverse CDF over weights w[0..V) in id order; records the margin.
-      auto draw = [&](const std::vector<double>& w, double u) -> int32_t {
-        double total = 0.0;
-        for (int64_t v = 0; v < V; ++v) total += w[v];
-        const double target_mass = u * total;
-        double run = 0.0, prev_run = 0.0;
-        int64_t chosen = -1;
+      // inverse CDF over integer weights w in id order (total > 0); records the margin
+      auto draw = [&](const std::vector<uint64_t>& w, uint64_t total, uint64_t U) -> int32_t {
+        const uint64_t tgt = scaled_target(U, total);
+        uint64_t run = 0;
         for (int64_t v = 0; v < V; ++v) {
-          prev_run = run;
+          const uint64_t prev = run;
           run += w[v];
-          if (target_mass < run) {
-            chosen = v;
-            break;
+          if (tgt < run) {
+            const double gap = static_cast<double>(std::min(run - tgt, tgt - prev + 1));
+            draw_margin = std::min(draw_margin, gap / static_cast<double>(total));
+            return static_cast<int32_t>(v);
           }
         }
-        if (chosen < 0) {
-          for (int64_t v = V - 1; v >= 0; --v)
-            if (w[v] > 0.0) {
-              chosen = v;
-              break;
-            }
-          prev_run = run;
-        }
-        double gap = std::min(run - target_mass, target_mass - prev_run);
-        draw_margin = std::min(draw_margin, gap / total);
-        return static_cast<int32_t>(chosen);
+        return static_cast<int32_t>(V - 1);   // not reached: tgt < total
       };
       n = L;
       for (int64_t t = 0; t < L; ++t) {
-        softmax_row(t);
+        const uint64_t Z = fixed_row_weights(row_of(t), V, c, W.data());
         const int32_t x = draft_tok[b * L + t];
-        const double qx = static_cast<double>(draft_q[(b * L + t) * K + draft_slot[b * L + t]]);
-        const double px = (x >= 0 && x < V) ? p[x] : 0.0;
-        const double u = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 1, offset);
-        const double lhs = u * qx;
-        accept_margin = std::min(accept_margin, std::fabs(lhs - px) / std::max(px, 1e-300));
-        if (lhs < px) continue;
-        std::vector<double> resid(p);
-        for (int64_t j = 0; j < K; ++j) {
-          const int32_t v = cand_idx[(b * L + t) * K + j];
-          if (v >= 0 && v < V)
-            resid[v] = std::max(0.0, p[v] - static_cast<double>(draft_q[(b * L + t) * K + j]));
-        }
+        int64_t slot = draft_slot[b * L + t];
+        slot = slot < 0 ? 0 : (slot >= K ? K - 1 : slot);
+        const double qx = static_cast<double>(draft_q[(b * L + t) * K + slot]);
+        const uint64_t Wx = (x >= 0 && x < V) ? W[x] : 0;
+        const double u1 = uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 1, offset);
+        const double lhs = (u1 * qx) * static_cast<double>(Z);
+        const double rhs = static_cast<double>(Wx);
+        accept_margin = std::min(accept_margin, std::fabs(lhs - rhs) / std::max(rhs, 1e-300));
+        if (lhs < rhs) continue;
         n = t;
-        last = draw(resid, uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 2, offset));
+        const uint64_t U2 = uniform24_bits(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(t), 2, offset);
+        if (Z == 0) {
+          last = argmax_row(t);
+          break;
+        }
+        // residual: each candidate slot takes Q_j off its (clamped) id
+        std::fill(Qs.begin(), Qs.end(), 0);
+        std::fill(is_cand.begin(), is_cand.end(), 0);
+        for (int64_t j = 0; j < K; ++j) {
+          const int64_t v = clamp_id(cand_idx[(b * L + t) * K + j], V, nullptr);
+          const float qj = draft_q[(b * L + t) * K + j];
+          const double qc = qj > 0.0f ? std::min(static_cast<double>(qj), 1.0) : 0.0;
+          Qs[v] += static_cast<uint64_t>(qc * static_cast<double>(Z));
+          is_cand[v] = 1;
+        }
+        uint64_t Rtot = 0;
+        for (int64_t v = 0; v < V; ++v) {
+          R[v] = is_cand[v] ? (W[v] > Qs[v] ? W[v] - Qs[v] : 0) : W[v];
+          Rtot += R[v];
+        }
+        last = Rtot > 0 ? draw(R, Rtot, U2) : draw(W, Z, U2);
         break;
       }
       if (n == L) {
-        softmax_row(L);
-        last = draw(p, uniform24(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(L), 2, offset));
+        const uint64_t Z = fixed_row_weights(row_of(L), V, c, W.data());
+        const uint64_t U2 = uniform24_bits(seed, static_cast<uint64_t>(b), static_cast<uint64_t>(L), 2, offset);
+        last = Z > 0 ? draw(W, Z, U2) : argmax_row(L);
       }
     }
     for (int64_t t = 0; t < n; ++t) out[t] = draft_tok[b * L + t];

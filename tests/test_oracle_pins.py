@@ -599,3 +599,174 @@ def test_exp2_neg_within_one_ulp_of_exact():
         got = oracle.exp2_neg(float(x))
         ref = math.exp2(float(x))
         assert abs(got - ref) <= 2.0**-23 * ref, (float(x), got, ref)
+
+
+# ---------------------------------------------------------------------------
+# reading R21: the sampled verification's fixed-point weights, and the fp32
+# walk, against plain fp64 restatements of the definitions
+# ---------------------------------------------------------------------------
+
+
+def test_verify_weights_are_floor_of_scaled_exp2():
+    rng = np.random.default_rng(40)
+    for T in (1.0, 0.6, 2.5):
+        row = f32_bits(rng.standard_normal(3000) * 3)
+        W, Z = oracle.verify_weights(row, T)
+        lf = synth.bf16_to_f32(row).astype(np.float64)
+        c = float(np.float32(1.44269504) / np.float32(T))
+        x = (lf - lf.max()) * c
+        exact = np.exp2(x) * 2.0**40
+        # the row's largest logit weighs exactly 2^40; every weight is floor(w 2^40)
+        # for an fp32 w within one fp32 ulp of 2^x, x = (l - M) c carrying one
+        # fp32 rounding (relative 2^-24, so 2^x moves by ln 2 |x| 2^-24 relative)
+        assert int(W[np.argmax(lf)]) == 2**40
+        err = np.abs(W.astype(np.float64) - exact)
+        assert np.all(err <= exact * (np.abs(x) * 2.0**-24 + 2.0**-23) + 1.0)
+        assert Z == int(np.sum(W.astype(object)))   # exact integer sum, any order
+
+
+def test_verify_weights_nan_and_degenerate_rows():
+    row = f32_bits(np.array([1.0, np.nan, 3.0, -np.inf, 3.0], np.float32))
+    W, Z = oracle.verify_weights(row, 1.0)
+    assert W[1] == 0 and W[3] == 0 and W[2] == 2**40 and W[4] == 2**40 and Z == int(W.sum())
+    for bad in (np.full(8, np.nan, np.float32), np.full(8, -np.inf, np.float32)):
+        W, Z = oracle.verify_weights(f32_bits(bad), 1.0)
+        assert Z == 0
+
+
+def test_verify_no_finite_logit_emits_the_argmax():
+    # Z = 0: the accept test fails (0 < 0 is false) and the token is the row's
+    # arg-max in top-k order (all NaN or all -inf: id 0; one +inf: that id)
+    V, L = 32, 1
+    rows = np.zeros((3, L + 1, V), np.float32)
+    rows[0, 0] = np.nan
+    rows[1, 0] = -np.inf
+    rows[2, 0] = -np.inf
+    rows[2, 0, 7] = np.inf
+    tg = f32_bits(rows)
+    ci = np.broadcast_to(np.arange(K, dtype=np.int32), (3, L, K)).copy()
+    q = np.full((3, L, K), 1.0 / K, np.float32)
+    acc, out, _ = oracle.verify(tg, np.ones((3, L), np.int32), np.ones((3, L), np.int32), q, ci,
+                                temperature=1.0, seed=2)
+    assert list(acc) == [1, 1, 1] and list(out[:, 0]) == [0, 0, 7]
+
+
+def _fp64_verify(tg_bits, tok, slot, q, ci, T, seed, offset):
+    """The plain definition in fp64 (softmax by np.exp, residual max(0, p - q),
+    inverse CDF in id order) with each decision's margin."""
+    B, L1, V = tg_bits.shape
+    L = L1 - 1
+    acc = np.zeros(B, np.int32)
+    out = np.full((B, L1), -1, np.int32)
+    margin = np.full(B, np.inf)
+
+    def p_of(b, t):
+        z = synth.bf16_to_f32(tg_bits[b, t]).astype(np.float64) / T
+        e = np.exp(z - z.max())
+        return e / e.sum()
+
+    def draw(w, u, b):
+        cdf = np.cumsum(w)
+        tgt = u * cdf[-1]
+        v = int(np.searchsorted(cdf, tgt, side="right"))
+        lo = cdf[v - 1] if v > 0 else 0.0
+        margin[b] = min(margin[b], min(cdf[v] - tgt, tgt - lo) / cdf[-1])
+        return v
+
+    for b in range(B):
+        n = L
+        for t in range(L):
+            p = p_of(b, t)
+            qx = float(q[b, t, slot[b, t]])
+            u1 = oracle.uniform24(seed, b, t, 1, offset)
+            margin[b] = min(margin[b], abs(u1 * qx - p[tok[b, t]]) / p[tok[b, t]])
+            if u1 * qx < p[tok[b, t]]:
+                continue
+            r = p.copy()
+            for j in range(K):
+                r[ci[b, t, j]] = max(0.0, p[ci[b, t, j]] - float(q[b, t, j]))
+            n = t
+            out[b, t] = draw(r, oracle.uniform24(seed, b, t, 2, offset), b)
+            break
+        if n == L:
+            out[b, L] = draw(p_of(b, L), oracle.uniform24(seed, b, L, 2, offset), b)
+        out[b, :n] = tok[b, :n]
+        acc[b] = n + 1
+    return acc, out, margin
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_verify_fixed_point_agrees_with_fp64_definition(T):
+    # R21's integer decisions equal the fp64 definition's wherever the latter is
+    # not within 1e-9 (relative) of a boundary: the fixed point changes no
+    # decision that floating point can resolve
+    rng = np.random.default_rng(41)
+    B, L, V = 300, 4, 600
+    S = (rng.standard_normal((B, L, K, K)) * 2).astype(np.float32)
+    ci = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(L)]) for _ in range(B)]).astype(np.int32)
+    tok, slot, q, _ = oracle.walk(S, ci, temperature=T, seed=3)
+    tg = synth.target_planted(42, tok, V, agree=0.7, plant=3.0)
+    acc, out, _ = oracle.verify(tg, tok, slot, q, ci, temperature=T, seed=4, offset=1)
+    facc, fout, fmargin = _fp64_verify(tg, tok, slot, q, ci, T, 4, 1)
+    ok = fmargin > 1e-9
+    assert ok.sum() >= B - 2
+    assert np.array_equal(acc[ok], facc[ok]) and np.array_equal(out[ok], fout[ok])
+    assert 1.0 < acc.mean() < L + 1
+
+
+def test_walk_fp32_agrees_with_fp64_definition():
+    # R5's fp32 draw against w = exp((S - max) / T) in fp64: equal except where
+    # u Z lies within 1e-6 Z of a CDF boundary
+    rng = np.random.default_rng(43)
+    B, L = 400, 8
+    for T in (1.0, 0.5, 2.0):
+        S = (rng.standard_normal((B, L, K, K)) * 2).astype(np.float32)
+        ci = rng.integers(0, 1000, (B, L, K)).astype(np.int32)
+        _, slot, _, _ = oracle.walk(S, ci, temperature=T, seed=7, offset=2)
+        checked = 0
+        for b in range(B):
+            prev = 0
+            for t in range(L):
+                s = S[b, t, prev].astype(np.float64)
+                w = np.exp((s - s.max()) / T)
+                cdf = np.cumsum(w)
+                tgt = oracle.uniform24(7, b, t, 0, 2) * cdf[-1]
+                if np.min(np.abs(cdf - tgt)) < 1e-6 * cdf[-1]:
+                    break   # later steps follow a predecessor that may legitimately differ
+                assert slot[b, t] == int(np.searchsorted(cdf, tgt, side="right")), (T, b, t)
+                checked += 1
+                prev = slot[b, t]
+        assert checked >= 0.99 * B * L
+
+
+def test_walk_nan_scores_never_win():
+    # greedy: the lowest slot of the largest non-NaN score (numpy's nanargmax);
+    # all NaN: slot 0.  Sampled: a NaN slot has q = 0; a row without a positive
+    # weight (all NaN or -inf) takes the greedy slot with q one-hot.
+    rng = np.random.default_rng(44)
+    B, L = 64, 6
+    S = rng.standard_normal((B, L, K, K)).astype(np.float32)
+    S[rng.random(S.shape) < 0.3] = np.nan
+    S[0, 0, 0, :] = np.nan
+    S[1, 0, 0, :] = -np.inf
+    S[2, 0, 0, 0] = np.nan
+    ci = rng.integers(0, 1000, (B, L, K)).astype(np.int32)
+    _, slot, q, _ = oracle.walk(S, ci)
+    for b in range(B):
+        prev = 0
+        for t in range(L):
+            row = S[b, t, prev]
+            expect = 0 if np.all(np.isnan(row)) else int(np.nanargmax(row))
+            assert slot[b, t] == expect
+            prev = expect
+    _, slot1, q1, _ = oracle.walk(S, ci, temperature=1.0, seed=3)
+    assert slot1[0, 0] == 0 and q1[0, 0, 0] == 1.0 and q1[0, 0].sum() == 1.0
+    assert slot1[1, 0] == 0 and q1[1, 0, 0] == 1.0
+    for b in range(B):
+        prev = 0
+        for t in range(L):
+            row = S[b, t, prev]
+            if not np.all(np.isnan(row) | np.isneginf(row)):
+                assert np.all(q1[b, t][np.isnan(row)] == 0.0)
+                assert not np.isnan(row[slot1[b, t]])
+            prev = slot1[b, t]
