@@ -245,6 +245,7 @@ class Cycle:
         self.acc = [torch.empty((nb,), dtype=torch.int32, device=dev) for _ in range(2)]
         self.out = [torch.empty((nb, L + 1), dtype=torch.int32, device=dev) for _ in range(2)]
         self.target = None
+        self.vws = torch.empty(api.verify_workspace(h, nb, L, V), dtype=torch.uint8, device=dev)
         # conv x10, top-16, gate + pairs, then per temperature: walk + verify (init + one cooperative kernel)
         self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 2)
 
@@ -265,7 +266,7 @@ class Cycle:
                      draft_slot=self.slot[i], draft_q=self.q[i])
             rec(f"walk{i}")
             api.verify(h, self.target, self.tok[i], self.slot[i], self.q[i], ci, temperature=T, seed=1,
-                       offset=seed_offset, accept_len=self.acc[i], out_tok=self.out[i])
+                       offset=seed_offset, accept_len=self.acc[i], out_tok=self.out[i], workspace=self.vws)
             rec(f"verify{i}")
 
 

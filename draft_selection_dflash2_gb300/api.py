@@ -216,19 +216,29 @@ def gemm_conv2tap(h: Handle, A, W, x_prev, hs, k0, k1, W_c, b_c=None, c_work=Non
     return y, c_work.view(-1)[: B * L * n].view(B * L, n)
 
 
+def verify_workspace(h: Handle, B: int, L: int, V: int) -> int:
+    return int(h._lib.dflash2_verify_workspace(h.ptr, B, L, V))
+
+
 def verify(h: Handle, target, draft_tok, draft_slot=None, draft_q=None, cand_idx=None,
            temperature: float = 0.0, seed: int = 0, offset: int = 0, V: int = None,
-           accept_len=None, out_tok=None, stream=None):
-    """target [B, L+1, V(ld)] bf16 -> (accept_len int32 [B], out_tok int32 [B, L+1])."""
+           accept_len=None, out_tok=None, workspace=None, stream=None):
+    """target [B, L+1, V(ld)] bf16 -> (accept_len int32 [B], out_tok int32 [B, L+1]).
+
+    workspace: device bytes (uint8 tensor) of at least verify_workspace(h, B, L, V);
+    allocated here by torch when None."""
     B, L1 = target.shape[0], target.shape[1]
     ld = target.stride(1)
     V = target.shape[2] if V is None else V
     dev = target.device
     accept_len = torch.empty((B,), dtype=torch.int32, device=dev) if accept_len is None else accept_len
     out_tok = torch.empty((B, L1), dtype=torch.int32, device=dev) if out_tok is None else out_tok
+    if workspace is None:
+        workspace = torch.empty(max(verify_workspace(h, B, L1 - 1, V), 256), dtype=torch.uint8, device=dev)
     _check(h._lib.dflash2_verify(h.ptr, _ptr(target), ld, _ptr(draft_tok), _ptr(draft_slot), _ptr(draft_q),
                                  _ptr(cand_idx), B, L1 - 1, V, float(temperature), seed, offset,
-                                 _ptr(accept_len), _ptr(out_tok), _stream(stream)), "dflash2_verify")
+                                 _ptr(accept_len), _ptr(out_tok), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)), "dflash2_verify")
     return accept_len, out_tok
 
 
@@ -306,3 +316,14 @@ def lmhead_topk_noalloc(h: Handle, hidden, W, vals=None, idx=None, stream=None):
                                               _stream(stream)), "dflash2_lmhead_topk_noalloc")
     return vals, idx
 
+
+
+def selftest_wait_timeout(h: Handle, limit_ns: int, words=None, stream=None):
+    """Runs the library's bounded-wait self-test: one kernel whose two waits
+    cannot be satisfied gives up after limit_ns each.  Returns the result word
+    (bit 2 = the kernel reached its end; bits 0/1 = a wait was satisfied)."""
+    if words is None:
+        words = torch.zeros(2, dtype=torch.int32, device=torch.device("cuda", h.device))
+    _check(h._lib.dflash2_selftest_wait_timeout(h.ptr, int(limit_ns), _ptr(words), _stream(stream)),
+           "dflash2_selftest_wait_timeout")
+    return words

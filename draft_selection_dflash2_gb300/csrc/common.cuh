@@ -31,6 +31,7 @@ __device__ __forceinline__ int32_t clamp_token(int32_t id, int64_t V, uint32_t* 
 }
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 // Programmatic dependent launch.  pdl_wait blocks until the grid this one was
 // launched after has completed and its writes are visible (a no-op when the
@@ -92,14 +93,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, giving up after kWaitLimitNs.
+// Waits for phase `parity` of `bar` to complete, giving up after limit_ns.
 // Returns false (and raises DFLASH2_DEVERR_TIMEOUT) if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - start > kWaitLimitNs) {
+    if ((it & 63u) == 0 && global_timer_ns() - start > limit_ns) {
+      raise_error(err, DFLASH2_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Waits until the word at `flag` (written by another CTA) reaches `value`,
+// giving up after limit_ns.  Returns false (and raises DFLASH2_DEVERR_TIMEOUT)
+// if it gave up.
+__device__ __forceinline__ bool flag_wait_bounded(const volatile uint32_t* flag, uint32_t value, uint32_t* err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (*flag >= value) return true;
+  const uint64_t start = global_timer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (*flag >= value) return true;
+    if (global_timer_ns() - start > limit_ns) {
       raise_error(err, DFLASH2_DEVERR_TIMEOUT);
       return false;
     }
@@ -157,6 +176,13 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) { return __uint_as_float(bits << 16); }
+
+// Order-preserving image of an fp32 score: NaN -> 0 (below -inf), -0 == +0.
+__device__ __forceinline__ uint32_t score_order(float v) {
+  if (v != v) return 0u;
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // ---------------------------------------------------------------------------
 // warp-level top-16 over 64-bit keys (one key per lane)

@@ -79,16 +79,17 @@ cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t
 cudaError_t launch_selector_eval(const int32_t* gt, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* accept1,
                                  int32_t* accept16, int64_t* counts, int num_sms, cudaStream_t stream);
 
-// Device scratch (work queue, per-row arrival counters, per-chunk partials)
-// that launch_verify needs for B sequences of L positions over a V-id vocabulary.
-size_t verify_scratch_bytes(int64_t B, int64_t L, int64_t V);
+// Device workspace (barrier words, per-row arrival counters, row maxima and
+// sums, per-chunk sums) that launch_verify needs for B sequences of L
+// positions over a V-id vocabulary, at either temperature.
+size_t verify_workspace_bytes(int64_t B, int64_t L, int64_t V);
 // Largest vocabulary launch_verify handles (10,485,760 ids).
 int64_t verify_max_vocab();
 
 cudaError_t launch_verify(const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                           const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
                           int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,
-                          uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* scratch,
+                          uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* workspace,
                           uint32_t* err, int num_sms, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t V, int64_t d, int num_sms);
@@ -112,6 +113,11 @@ cudaError_t launch_pair_scores_proj(const int32_t* cand_idx, const float* cand_v
                                     const float* gate, const uint16_t* E, const uint16_t* W_A, const uint16_t* W_B,
                                     int64_t B, int64_t L, int64_t d, int64_t V, float* P, float* S, int num_sms,
                                     uint32_t* err, cudaStream_t stream);
+// A kernel whose two bounded waits (an mbarrier, a global word) cannot be
+// satisfied; each gives up after limit_ns (selftest.cu).
+cudaError_t launch_wait_timeout_selftest(const uint32_t* flag, uint64_t limit_ns, uint32_t* err, uint32_t* result,
+                                         cudaStream_t stream);
+
 constexpr size_t kLmheadNoAllocScratchBytes = DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES;
 cudaError_t lmhead_noalloc_scratch(int device, void** ptr);
 cudaError_t launch_lmhead_topk(const uint16_t* hidden, const uint16_t* W, int64_t M, int64_t V,

@@ -33,14 +33,20 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
   out[3] = c3;
 }
 
-// Uniform in [0, 1) with 24 random bits, as a double (exact).
-__device__ __forceinline__ double philox_uniform24(uint64_t seed, uint32_t b, uint32_t t,
-                                                   uint32_t stream, uint64_t offset) {
+// The 24 random bits of (b, t, stream, offset) under key seed: x0 >> 8.
+__device__ __forceinline__ uint32_t philox_bits24(uint64_t seed, uint32_t b, uint32_t t, uint32_t stream,
+                                                  uint64_t offset) {
   uint32_t out[4];
   philox4x32_10(b, t | (stream << 24), static_cast<uint32_t>(offset),
                 static_cast<uint32_t>(offset >> 32), static_cast<uint32_t>(seed),
                 static_cast<uint32_t>(seed >> 32), out);
-  return static_cast<double>(out[0] >> 8) * (1.0 / 16777216.0);
+  return out[0] >> 8;
+}
+
+// Uniform in [0, 1) with 24 random bits, as a double (exact).
+__device__ __forceinline__ double philox_uniform24(uint64_t seed, uint32_t b, uint32_t t,
+                                                   uint32_t stream, uint64_t offset) {
+  return static_cast<double>(philox_bits24(seed, b, t, stream, offset)) * (1.0 / 16777216.0);
 }
 
 }  // namespace dflash2

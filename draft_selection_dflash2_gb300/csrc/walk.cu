@@ -9,7 +9,8 @@
 // computes the L Philox uniforms in parallel, one step per lane, so the L
 // dependent steps touch neither global memory nor Philox.  Lane j (j < 16)
 // owns successor slot j.
-//   greedy : shuffle arg-max over (value, lowest slot).
+//   greedy : shuffle arg-max over (value, lowest slot), a NaN score below
+//            every number (all NaN: slot 0).
 //   sampled: everything in fp32 (the draw is an integer decided by floating
 //            point): c = log2(e) / T, w_j = exp2_neg((S_j - max) * c), Z and the
 //            CDF summed in slot order, u the Philox uniform of (b, t, stream 0)
@@ -18,31 +19,15 @@
 //            degree-7 Taylor polynomial, and every step is a correctly rounded
 //            IEEE operation (explicit _rn intrinsics, no contraction), so the
 //            draw is reproducible by any implementation of the same steps.
+//            A row with no positive weight (every score NaN or -inf) takes the
+//            greedy slot, with q one-hot there.
 #include "common.cuh"
+#include "exp2.cuh"
 #include "launch.h"
 #include "philox.cuh"
 
 namespace dflash2 {
 namespace {
-
-// 2^x for x <= 0 in fp32: x = n + f, n = rint(x), f in [-1/2, 1/2]; 2^f by the
-// degree-7 Taylor polynomial of e^(f ln 2) (coefficients (ln 2)^k / k! rounded
-// to fp32) in Horner form with fused multiply-adds; times 2^n (exact scaling,
-// correctly rounded when the result is subnormal); 0 below -126 and for NaN.
-__device__ __forceinline__ float exp2_neg(float x) {
-  if (!(x >= -126.0f)) return 0.0f;
-  const float n = rintf(x);
-  const float f = __fsub_rn(x, n);
-  float p = 1.525273365e-05f;
-  p = __fmaf_rn(p, f, 1.540352969e-04f);
-  p = __fmaf_rn(p, f, 1.333355787e-03f);
-  p = __fmaf_rn(p, f, 9.618128650e-03f);
-  p = __fmaf_rn(p, f, 5.550410971e-02f);
-  p = __fmaf_rn(p, f, 2.402265072e-01f);
-  p = __fmaf_rn(p, f, 6.931471825e-01f);
-  p = __fmaf_rn(p, f, 1.0f);
-  return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
-}
 
 constexpr int kWalkWarps = 2;            // sequences per CTA (2 x 69 KB at L = 64)
 constexpr int kMaxWalkL = 64;
@@ -96,18 +81,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   int prev = 0;
   for (int64_t t = 0; t < L; ++t) {
     const float v = sb[(t * kTopK + prev) * kTopK + j];
-    // arg-max with the lowest slot on ties (lanes 16..31 mirror 0..15)
-    float bv = v;
-    int bj = j;
+    // arg-max under one total order, so every lane reaches the same slot: the
+    // score's order image (NaN lowest, -0 == +0) above 15 - slot (lowest slot
+    // first on ties); lanes 16..31 mirror 0..15
+    uint64_t key = (static_cast<uint64_t>(score_order(v)) << 32) | static_cast<uint32_t>(kTopK - 1 - j);
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, o);
-      if (ov > bv || (ov == bv && oj < bj)) {
-        bv = ov;
-        bj = oj;
-      }
-    }
+    for (int o = 8; o > 0; o >>= 1) key = kmax(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
+    const int bj = kTopK - 1 - static_cast<int>(key & 0xFu);
+    const float bv = __shfl_sync(0xFFFFFFFFu, v, bj);
     int chosen;
     const int64_t q_at = (b * L + t) * kTopK + j;
     if (temperature <= 0.0f) {
@@ -124,21 +105,27 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
         Z = __fadd_rn(Z, __shfl_sync(0xFFFFFFFFu, w, i));
         cdf[i] = Z;
       }
-      const float target = __fmul_rn(us[t], Z);
-      int pick = -1;
+      if (!(Z > 0.0f)) {
+        // no positive weight (every score NaN or -inf): the greedy slot
+        chosen = bj;
+        if (draft_q && lane < kTopK) draft_q[q_at] = (j == chosen) ? 1.0f : 0.0f;
+      } else {
+        const float target = __fmul_rn(us[t], Z);
+        int pick = -1;
 #pragma unroll
-      for (int i = kTopK - 1; i >= 0; --i)
-        if (target < cdf[i]) pick = i;
-      if (pick < 0) {
-        // u Z below every partial sum cannot fail for u < 1; keep the last positive weight
         for (int i = kTopK - 1; i >= 0; --i)
-          if (cdf[i] > (i > 0 ? cdf[i - 1] : 0.0f)) {
-            pick = i;
-            break;
-          }
+          if (target < cdf[i]) pick = i;
+        if (pick < 0) {
+          // u Z below every partial sum cannot fail for u < 1; keep the last positive weight
+          for (int i = kTopK - 1; i >= 0; --i)
+            if (cdf[i] > (i > 0 ? cdf[i - 1] : 0.0f)) {
+              pick = i;
+              break;
+            }
+        }
+        chosen = pick;
+        if (draft_q && lane < kTopK) draft_q[q_at] = __fdiv_rn(w, Z);
       }
-      chosen = pick;
-      if (draft_q && lane < kTopK) draft_q[q_at] = __fdiv_rn(w, Z);
     }
     if (lane == 0) {
       draft_slot[b * L + t] = chosen;

@@ -78,7 +78,8 @@ def main():
         target = bf(torch, synth.target_planted(5, tok, V, agree=0.85, plant=8.0))
         dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
         tok_d, slot_d, q_d, ci_d = dev(tok), dev(slot), dev(q), dev(ci)
-        run = lambda: api.verify(h, target, tok_d, slot_d, q_d, ci_d, temperature=T, seed=1)  # noqa: E731
+        ws = torch.empty(api.verify_workspace(h, B, L, V), dtype=torch.uint8, device="cuda")
+        run = lambda: api.verify(h, target, tok_d, slot_d, q_d, ci_d, temperature=T, seed=1, workspace=ws)  # noqa: E731
     elif args.stage == "viterbi":
         g = torch.Generator(device="cuda")
         g.manual_seed(5)

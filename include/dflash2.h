@@ -19,9 +19,14 @@
  * Conventions for every call
  *   - Pointers marked "device" are CUDA device pointers on the handle's device;
  *     "host" pointers are ordinary host memory.  The caller owns every buffer:
- *     the library never frees a pointer or keeps one past the call, and no call
- *     on the compute path allocates memory, except dflash2_verify when it needs
- *     more scratch than the handle holds (see there).
+ *     the library never frees a pointer or keeps one past the call.  The only
+ *     allocation the library makes is the handle's 4-byte error word, in
+ *     dflash2_create; calls that need scratch take a caller workspace whose
+ *     size a *_workspace query gives (dflash2_lmhead_topk_noalloc uses a fixed
+ *     array inside the library instead).
+ *   - The handle's device must be the calling thread's current device
+ *     (cudaSetDevice); a compute call made while another device is current
+ *     returns DFLASH2_ERR_INVALID_ARG before anything launches.
  *   - bf16 tensors are passed as `const uint16_t*` holding bf16 bit patterns.
  *   - Tensors are row-major and contiguous unless an explicit leading dimension
  *     (`ld`, in elements) is given.  bf16 base pointers must be 16-byte aligned
@@ -54,7 +59,7 @@ typedef struct dflash2_handle dflash2_handle;
 enum dflash2_status {
   DFLASH2_OK = 0,
   DFLASH2_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent size      */
-  DFLASH2_ERR_UNSUPPORTED = -2, /* k != 16, V < 16, d % 16 != 0, L > 64, ...         */
+  DFLASH2_ERR_UNSUPPORTED = -2, /* k != 16, V < 16, d % 64 != 0, L > 64, ...         */
   DFLASH2_ERR_MISALIGNED = -3,  /* a pointer or leading dimension breaks alignment  */
   DFLASH2_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed      */
   DFLASH2_ERR_TIMEOUT = -5,     /* a bounded device wait gave up (see error word)   */
@@ -75,8 +80,8 @@ const char* dflash2_status_string(int status);
 
 /*
  * Creates a handle bound to CUDA device `device`.  Allocates the 4-byte device
- * error word (the only allocation the library ever makes) and records the SM
- * count.  Makes `device` current on the calling thread.
+ * error word (the library's only allocation) and records the SM count.  Makes
+ * `device` current on the calling thread.
  */
 int dflash2_create(int device, dflash2_handle** out);
 
@@ -88,7 +93,8 @@ int dflash2_num_sms(const dflash2_handle* h);
 
 /*
  * Synchronises `stream`, copies the device error word to *bits (host) and, if
- * `clear` is non-zero, resets it to 0.
+ * `clear` is non-zero, resets it to 0 (without `clear` a caller can poll the
+ * word and leave its bits for another reader).
  */
 int dflash2_get_device_error(dflash2_handle* h, void* stream, uint32_t* bits, int clear);
 
@@ -166,13 +172,15 @@ int dflash2_pair_scores_proj(dflash2_handle* h, const int32_t* cand_idx, const f
  * last verified token, greedy follows the best successor at each step and
  * sampling draws from the same scores.  Step t reads row 0 of S[b,0] at t = 0
  * and row draft_slot[b,t-1] afterwards.
- *   temperature <= 0: slot = lowest j maximising the row; draft_q one-hot.
+ *   temperature <= 0: slot = lowest j maximising the row, a NaN score below
+ *     every number (all NaN: slot 0); draft_q one-hot.
  *   temperature  > 0: every step in fp32 with correctly rounded operations:
  *     w_j = 2^((S_j - max S) * (log2(e) / T)) (Cody-Waite reduction and a
  *     degree-7 Taylor polynomial), Z summed in slot order, u = Philox4x32-10
  *     uniform of counter (b, t | 0 << 24, offset_lo, offset_hi), key (seed_lo,
  *     seed_hi), u = (x0 >> 8) * 2^-24; slot = smallest j with
- *     u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.
+ *     u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.  A row with no positive
+ *     weight (every score NaN or -inf) takes the greedy slot, q one-hot there.
  *   S          device fp32 [B, L, 16, 16], 16-byte aligned (each sequence's
  *              block is staged in shared memory by one bulk copy)
  *   cand_idx   device int32 [B, L, 16]
@@ -270,31 +278,42 @@ int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* 
  * Block verification against the target's logits.  "A Lightweight Path
  * Selector" (rejection sampling restores the exact target distribution) and
  * Table 1's note (the acceptance length includes the verifier's next token).
- *   temperature <= 0: a_t = argmax target[b,t,:] (lowest id on ties);
- *     n = first t < L with draft_tok[b,t] != a_t (else L);
+ *   temperature <= 0: a_t = argmax target[b,t,:] (lowest id on ties, NaN below
+ *     -inf);  n = first t < L with draft_tok[b,t] != a_t (else L);
  *     out_tok[b] = draft_tok[b,0..n-1], a_n, then -1;  accept_len[b] = n + 1.
- *   temperature  > 0: speculative rejection sampling with p_t = softmax(target_t/T)
- *     and q_t = draft_q[b,t,:] on cand_idx[b,t,:] (zero elsewhere): accept t iff
- *     u1 q_t(x_t) < p_t(x_t); on the first rejection draw from max(0, p_t - q_t)
- *     by inverse CDF in id order with u2; after L acceptances draw the bonus from
- *     p_L with u2 at t = L.  u1, u2 are the Philox uniforms of streams 1 and 2.
+ *   temperature  > 0: speculative rejection sampling with p_t in exact fixed
+ *     point: c = log2(e) / T (fp32), M = the row's largest non-NaN logit,
+ *     W_v = floor(exp2_neg((l_v - M) c) 2^40) (the fp32 2^x of dflash2_walk),
+ *     Z = sum_v W_v, p_t(v) = W_v / Z, an exact integer ratio whatever the
+ *     order of the parallel sums.  With q = draft_q[b,t,draft_slot[b,t]]:
+ *     accept t iff (u1 q) Z < W_x in fp64 (x = draft_tok[b,t]).  On the first
+ *     rejection draw from R_v = max(0, W_v - sum_{j: cand_idx[b,t,j] = v} Q_j),
+ *     Q_j = floor(min(draft_q[b,t,j], 1) Z), by inverse CDF in id order with the
+ *     target floor(U2 R / 2^24), R = sum_v R_v (from W if R = 0); after L
+ *     acceptances draw the bonus from W of row L the same way.  u1 = U1 2^-24
+ *     and U2 are the 24-bit Philox integers of streams 1 and 2 at (b, t); a
+ *     row with no finite logit (Z = 0) rejects and emits its arg-max.
  *   target      device bf16 [B, L+1, ld] (row (b,t) at (b*(L+1)+t)*ld)
  *   draft_tok, draft_slot  device int32 [B, L];  draft_q device fp32 [B, L, 16]
  *   cand_idx    device int32 [B, L, 16]
  *   accept_len  device int32 [B];  out_tok device int32 [B, L+1]
+ *   workspace   device scratch of at least dflash2_verify_workspace(h, B, L, V)
+ *               bytes, 256-byte aligned (barrier words, per-row counters, maxima
+ *               and sums, per-chunk sums), fully re-initialised by every call;
+ *               calls that overlap on the GPU must not share it.
  * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0, and every
  * draft argument may be NULL when L = 0 (only the bonus row is decided).
- * L <= 64, V <= 10,485,760 (DFLASH2_ERR_UNSUPPORTED beyond).
- * The call keeps per-row scratch in the handle (1 MiB from dflash2_create;
- * 12 bytes per target row, plus 16 bytes per 4096 vocabulary ids at T > 0).  A call that needs more allocates a larger buffer,
- * after synchronising the device; under stream capture it cannot, and returns
- * DFLASH2_ERR_WORKSPACE instead, so make one call of the largest B * (L+1)
- * before capturing.  Calls on one handle must not overlap on the GPU.
+ * L <= 64, V <= 10,485,760 (DFLASH2_ERR_UNSUPPORTED beyond).  A too-small or
+ * NULL workspace returns DFLASH2_ERR_WORKSPACE.  Out-of-range draft tokens,
+ * slots and candidate ids are clamped (a draft token outside [0, V) weighs 0)
+ * and flagged in the error word.
  */
+size_t dflash2_verify_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t V);
 int dflash2_verify(dflash2_handle* h, const uint16_t* target, int64_t ld, const int32_t* draft_tok,
                    const int32_t* draft_slot, const float* draft_q, const int32_t* cand_idx,
                    int64_t B, int64_t L, int64_t V, float temperature, uint64_t seed,
-                   uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* stream);
+                   uint64_t offset, int32_t* accept_len, int32_t* out_tok, void* workspace,
+                   size_t ws_bytes, void* stream);
 
 /*
  * Fused LM head + top-16: logits = hidden W^T are produced tile by tile on the
@@ -355,6 +374,22 @@ int dflash2_lmhead_topk_gate(dflash2_handle* h, const uint16_t* hidden, const ui
 #define DFLASH2_LMHEAD_NOALLOC_SCRATCH_BYTES (4u << 20)
 int dflash2_lmhead_topk_noalloc(dflash2_handle* h, const uint16_t* hidden, const uint16_t* W, int64_t M,
                                 int64_t V, int64_t d, float* vals, int32_t* idx, void* stream);
+
+/*
+ * Self-test of failure detection, run without a GPU fault.  The pages have no
+ * counterpart: every wait inside the library's kernels (an mbarrier that a TMA
+ * copy or tensor-core commit completes, a word another CTA writes) is bounded,
+ * and this call shows that a bound is kept.  It launches one kernel whose two
+ * waits cannot be satisfied -- an mbarrier no thread arrives on, and
+ * words[0] reaching 1, which no one writes -- each with limit `limit_ns`
+ * (0 < limit_ns <= 2e9, the library's own limit).  Each wait gives up, ORs
+ * DFLASH2_DEVERR_TIMEOUT into the error word, and the kernel returns normally,
+ * leaving the context usable.
+ *   words  device uint32 [2]: words[0] must hold 0 (the caller keeps it 0);
+ *          words[1] receives bit 0 / bit 1 if the mbarrier / word wait was
+ *          satisfied (never) and bit 2 when the kernel reached its end.
+ */
+int dflash2_selftest_wait_timeout(dflash2_handle* h, uint64_t limit_ns, uint32_t* words, void* stream);
 
 #ifdef __cplusplus
 }

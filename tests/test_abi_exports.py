@@ -38,7 +38,7 @@ def test_null_handle_is_rejected_without_a_device(lib):
     assert lib.dflash2_topk(null, one, 4, 64, 64, 16, one, one, null) == -1
     assert lib.dflash2_walk(null, one, one, 1, 4, 0.0, 0, 0, one, one, null, null) == -1
     assert lib.dflash2_verify(null, one, 64, one, null, null, null, 1, 4, 64, 0.0, 0, 0, one, one,
-                              null) == -1
+                              one, 1 << 20, null) == -1
     assert lib.dflash2_conv2tap(null, one, one, null, one, one, one, null, 1, 4, 64, one, 1, null) == -1
     assert lib.dflash2_pair_scores(null, one, one, one, one, one, null, one, one, 1, 4, 64, 64, one,
                                    one, null) == -1
@@ -46,6 +46,23 @@ def test_null_handle_is_rejected_without_a_device(lib):
     assert lib.dflash2_create(0, None) == -1
 
 
-def test_lmhead_workspace_query_is_host_only(lib):
+def test_workspace_queries_are_host_only(lib):
     null = ctypes.c_void_p(None)
     assert lib.dflash2_lmhead_topk_workspace(null, 1024, 151936, 5120) == 0
+    assert lib.dflash2_verify_workspace(null, 128, 16, 151936) == 0
+    assert lib.dflash2_gemm_conv2tap_workspace(null, 128, 16, 5120) == 0
+
+
+def test_handle_allocates_only_its_error_word():
+    # the library's only cudaMalloc is the handle's error word in dflash2_create
+    import os
+    import re
+    csrc = os.path.join(os.path.dirname(_lib.HERE), "draft_selection_dflash2_gb300", "csrc")
+    hits = []
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        for m in re.finditer(r"\bcudaMalloc\w*\s*\(", text):
+            hits.append((name, text[:m.start()].count("\n") + 1))
+    assert [h[0] for h in hits] == ["api.cu"], hits
+    api_src = open(os.path.join(csrc, "api.cu")).read()
+    assert api_src.count("cudaMalloc(") == 1 and "cudaMalloc(&h->err" in api_src

@@ -61,3 +61,29 @@ def test_walk_without_q(handle):
     assert q is None
     otok, oslot, _, _ = oracle.walk(S, ci, temperature=1.0, seed=3)
     assert np.array_equal(host(slot), oslot)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_walk_nan_scores(handle, T):
+    """NaN never beats a number (the lowest slot of the largest non-NaN score
+    wins; all NaN: slot 0), in any slot, at either temperature; a sampled row
+    with no positive weight (all NaN or -inf) takes the greedy slot with q
+    one-hot.  Every lane must reach the same slot, or later steps would mix
+    predecessors: slots, tokens and q are compared bit for bit."""
+    rng = np.random.default_rng(77)
+    B, L = 96, 12
+    S = rng.standard_normal((B, L, K, K)).astype(np.float32)
+    S[rng.random(S.shape) < 0.25] = np.nan
+    S[0, 0, 0, :] = np.nan
+    S[1, 0, 0, :] = -np.inf
+    S[2, 0, 0, 0] = np.nan
+    S[3, :, :, 7] = np.nan
+    S[4, 1] = np.nan
+    S[5, 2] = -np.inf
+    ci = rng.integers(0, 151936, (B, L, K)).astype(np.int32)
+    tok, slot, q = api.walk(handle, f32(S), i32(ci), temperature=T, seed=8)
+    otok, oslot, oq, _ = oracle.walk(S, ci, temperature=float(np.float32(T)), seed=8)
+    assert np.array_equal(host(slot), oslot) and np.array_equal(host(tok), otok)
+    assert np.array_equal(host(q).view(np.uint32), oq.view(np.uint32))
+    assert (oslot >= 0).all()
+    assert handle.device_error() == 0
