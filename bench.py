@@ -91,7 +91,7 @@ _PROFILED = {
 }
 _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
-    "conv2tap": ["conv2tap.cu", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
+    "conv2tap": ["conv2tap.cu", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
     "verify": ["verify.cu", "common.cuh", "philox.cuh"],
     "pair_scores": ["select.cu", "pair_math.cuh", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
     "proj": ["proj.cu", "pair_math.cuh", "tcgen05.cuh", "common.cuh"],
@@ -246,6 +246,7 @@ class Cycle:
         self.out = [torch.empty((nb, L + 1), dtype=torch.int32, device=dev) for _ in range(2)]
         self.target = None
         self.vws = torch.empty(api.verify_workspace(h, nb, L, V), dtype=torch.uint8, device=dev)
+        self.cws = torch.empty(api.conv2tap_workspace(h, nb, L, D), dtype=torch.uint8, device=dev)
         # conv x10, top-16, gate + pairs, then per temperature: walk + verify (init + one cooperative kernel)
         self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 2)
 
@@ -254,7 +255,7 @@ class Cycle:
         rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
         rec("start")
         for a, (x, xp, k0, k1, W) in enumerate(self.conv):
-            cur = api.conv2tap(h, x, xp, k0, k1, W, y=self.ybuf[a % 2])
+            cur = api.conv2tap(h, x, xp, k0, k1, W, y=self.ybuf[a % 2], workspace=self.cws)
         rec("conv")
         api.topk(h, self.U, vals=self.vals, idx=self.idx)
         rec("topk")

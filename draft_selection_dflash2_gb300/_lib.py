@@ -32,7 +32,8 @@ SIGNATURES = {
     "dflash2_walk": (I32, [P, P, P, I64, I64, F32, U64, U64, P, P, P, P]),
     "dflash2_walk_viterbi": (I32, [P, P, P, I64, I64, P, P, P, P]),
     "dflash2_selector_eval": (I32, [P, P, P, I64, I64, P, P, P, P]),
-    "dflash2_conv2tap": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, P, I32, P]),
+    "dflash2_conv2tap_workspace": (SZ, [P, I64, I64, I64]),
+    "dflash2_conv2tap": (I32, [P, P, P, P, P, P, P, P, I64, I64, I64, P, I32, P, SZ, P]),
     "dflash2_verify_workspace": (SZ, [P, I64, I64, I64]),
     "dflash2_verify": (I32, [P, P, I64, P, P, P, P, I64, I64, I64, F32, U64, U64, P, P, P, SZ, P]),
     "dflash2_lmhead_topk_workspace": (SZ, [P, I64, I64, I64]),

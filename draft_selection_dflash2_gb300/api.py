@@ -174,16 +174,26 @@ def selector_eval(h: Handle, gt, cand_idx, accept1=None, accept16=None, counts=N
     return accept1, accept16, counts
 
 
+def conv2tap_workspace(h: Handle, B: int, L: int, d: int) -> int:
+    return int(h._lib.dflash2_conv2tap_workspace(h.ptr, B, L, d))
+
+
 def conv2tap(h: Handle, x, x_prev, k0, k1, W_c, b_c=None, hs=None, y=None, y_fp32: bool = False,
-             stream=None):
-    """x [B, L, d] bf16 -> y [B, L, d] (bf16, or fp32 when y_fp32)."""
+             workspace=None, stream=None):
+    """x [B, L, d] bf16 -> y [B, L, d] (bf16, or fp32 when y_fp32).
+
+    workspace: device bytes (uint8 tensor) of at least conv2tap_workspace(h, B, L, d);
+    allocated here by torch when None."""
     B, L, d = x.shape
     dev = x.device
     if y is None:
         y = torch.empty((B, L, d), dtype=torch.float32 if y_fp32 else torch.bfloat16, device=dev)
     y_is_fp32 = 1 if y.dtype == torch.float32 else 0
+    if workspace is None:
+        workspace = torch.empty(max(conv2tap_workspace(h, B, L, d), 256), dtype=torch.uint8, device=dev)
     _check(h._lib.dflash2_conv2tap(h.ptr, _ptr(x), _ptr(x_prev), _ptr(hs), _ptr(k0), _ptr(k1), _ptr(W_c),
-                                   _ptr(b_c), B, L, d, _ptr(y), y_is_fp32, _stream(stream)),
+                                   _ptr(b_c), B, L, d, _ptr(y), y_is_fp32, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "dflash2_conv2tap")
     return y
 

@@ -211,20 +211,28 @@ int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* c
                                                     as_stream(stream)));
 }
 
+size_t dflash2_conv2tap_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d) {
+  if (bad_handle(h) || B <= 0 || L <= 0 || d <= 0 || d % 64 != 0) return 0;
+  return dflash2::conv_workspace_bytes(B, L, d, h->num_sms);
+}
+
 int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_prev,
                      const uint16_t* hs, const uint16_t* k0, const uint16_t* k1,
                      const uint16_t* W_c, const float* b_c, int64_t B, int64_t L, int64_t d,
-                     void* y, int y_is_fp32, void* stream) {
+                     void* y, int y_is_fp32, void* workspace, size_t ws_bytes, void* stream) {
   const NvtxRange range("dflash2_conv2tap");
   if (bad_handle(h) || B < 0 || L < 0 || d <= 0) return DFLASH2_ERR_INVALID_ARG;
   if (d % 64 != 0 || L > kMaxL || B > 65535) return DFLASH2_ERR_UNSUPPORTED;
   if (B == 0 || L == 0) return DFLASH2_OK;
   if (!x || !x_prev || !k0 || !k1 || !W_c || !y) return DFLASH2_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(x_prev, 16) || (hs && !aligned(hs, 16)) || !aligned(k0, 16) ||
-      !aligned(k1, 16) || !aligned(W_c, 16) || !aligned(y, 16) || (b_c && !aligned(b_c, 4)))
+      !aligned(k1, 16) || !aligned(W_c, 16) || !aligned(y, 16) || (b_c && !aligned(b_c, 4)) ||
+      (workspace && !aligned(workspace, 256)))
     return DFLASH2_ERR_MISALIGNED;
+  if (workspace == nullptr || ws_bytes < dflash2::conv_workspace_bytes(B, L, d, h->num_sms))
+    return DFLASH2_ERR_WORKSPACE;
   if (const int st = wrong_device(h)) return st;
-  return launched(dflash2::launch_conv2tap(x, x_prev, hs, k0, k1, W_c, b_c, B, L, d, y, y_is_fp32,
+  return launched(dflash2::launch_conv2tap(x, x_prev, hs, k0, k1, W_c, b_c, B, L, d, y, y_is_fp32, workspace,
                                            h->err, h->num_sms, as_stream(stream)));
 }
 

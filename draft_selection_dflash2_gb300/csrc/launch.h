@@ -68,10 +68,13 @@ cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int6
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
                         int32_t* draft_slot, float* draft_q, uint32_t* err, cudaStream_t stream);
 
+// The two-tap conv (conv2tap.cu): the correction's split-K partials go to the
+// workspace ([ks, B*L, 2d/16] fp32), then the taps.
+size_t conv_workspace_bytes(int64_t B, int64_t L, int64_t d, int num_sms);
 cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uint16_t* hs,
                             const uint16_t* k0, const uint16_t* k1, const uint16_t* W_c,
                             const float* b_c, int64_t B, int64_t L, int64_t d, void* y,
-                            int y_is_fp32, uint32_t* err, int num_sms, cudaStream_t stream);
+                            int y_is_fp32, void* workspace, uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_walk_viterbi(const float* S, const int32_t* cand_idx, int64_t B, int64_t L, int32_t* draft_tok,
                                 int32_t* draft_slot, float* score, uint32_t* err, cudaStream_t stream);

@@ -144,4 +144,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                        uint32_t box_rows);
 
+// A 3-D fp32 tensor map over a dense [d2][d1][d0] array (d0 innermost), box =
+// [box1, box0] in one d2 slice, with the 128-byte swizzle (box0 * 4 <= 128
+// bytes).  Boxes clip at every dimension's end, so a store never crosses
+// into the next d2 slice.  Returns false if the driver rejects it.
+bool make_tmap_f32_3d(CUtensorMap* map, void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                      uint32_t box1);
+
 }  // namespace dflash2

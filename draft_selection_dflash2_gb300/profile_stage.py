@@ -68,7 +68,8 @@ def main():
         xp = bf(torch, synth.normal_bits(2, (B, D)))
         k0, k1, W_c = (bf(torch, a) for a in synth.conv_layer_params(3, D))
         y = torch.empty((B, L, D), dtype=torch.bfloat16, device="cuda")
-        run = lambda: api.conv2tap(h, x, xp, k0, k1, W_c, y=y)  # noqa: E731
+        cws = torch.empty(api.conv2tap_workspace(h, B, L, D), dtype=torch.uint8, device="cuda")
+        run = lambda: api.conv2tap(h, x, xp, k0, k1, W_c, y=y, workspace=cws)  # noqa: E731
     elif args.stage in ("verify0", "verify1"):
         T = 0.0 if args.stage == "verify0" else 1.0
         tok = rng.integers(0, V, (B, L)).astype(np.int32)

@@ -239,12 +239,20 @@ int dflash2_selector_eval(dflash2_handle* h, const int32_t* gt, const int32_t* c
  *   k0, k1  device bf16 [d];  W_c device bf16 [2d/16, d];  b_c device fp32 [2d/16] or NULL
  *   y       device [B, L, d], fp32 if y_is_fp32 else bf16 (round to nearest even);
  *           must not overlap x, x_prev or hs.
- * d % 64 == 0, L <= 64, B <= 65535.
+ *   workspace  device scratch of at least dflash2_conv2tap_workspace(h, B, L, d)
+ *              bytes, 256-byte aligned: the correction's fp32 split-K partials
+ *              (a few per position and group), rewritten by every call; calls
+ *              that overlap on the GPU must not share it.  The size depends on
+ *              the device's SM count, hence the handle argument.
+ * The correction is summed over its K splits in a fixed order, so a call gives
+ * the same bits every time.  d % 64 == 0, L <= 64, B <= 65535.  A too-small or
+ * NULL workspace returns DFLASH2_ERR_WORKSPACE.
  */
+size_t dflash2_conv2tap_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d);
 int dflash2_conv2tap(dflash2_handle* h, const uint16_t* x, const uint16_t* x_prev,
                      const uint16_t* hs, const uint16_t* k0, const uint16_t* k1,
                      const uint16_t* W_c, const float* b_c, int64_t B, int64_t L, int64_t d,
-                     void* y, int y_is_fp32, void* stream);
+                     void* y, int y_is_fp32, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * The two-tap conv fused into the GEMM that produces its input (the output

@@ -39,7 +39,8 @@ def test_null_handle_is_rejected_without_a_device(lib):
     assert lib.dflash2_walk(null, one, one, 1, 4, 0.0, 0, 0, one, one, null, null) == -1
     assert lib.dflash2_verify(null, one, 64, one, null, null, null, 1, 4, 64, 0.0, 0, 0, one, one,
                               one, 1 << 20, null) == -1
-    assert lib.dflash2_conv2tap(null, one, one, null, one, one, one, null, 1, 4, 64, one, 1, null) == -1
+    assert lib.dflash2_conv2tap(null, one, one, null, one, one, one, null, 1, 4, 64, one, 1, one, 1 << 20,
+                                null) == -1
     assert lib.dflash2_pair_scores(null, one, one, one, one, one, null, one, one, 1, 4, 64, 64, one,
                                    one, null) == -1
     assert lib.dflash2_lmhead_topk(null, one, one, 4, 64, 64, one, one, one, 256, null) == -1
@@ -51,6 +52,7 @@ def test_workspace_queries_are_host_only(lib):
     assert lib.dflash2_lmhead_topk_workspace(null, 1024, 151936, 5120) == 0
     assert lib.dflash2_verify_workspace(null, 128, 16, 151936) == 0
     assert lib.dflash2_gemm_conv2tap_workspace(null, 128, 16, 5120) == 0
+    assert lib.dflash2_conv2tap_workspace(null, 128, 16, 5120) == 0
 
 
 def test_handle_allocates_only_its_error_word():
