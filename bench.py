@@ -93,7 +93,7 @@ _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
     "conv2tap": ["conv2tap.cu", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
     "verify": ["verify.cu", "common.cuh", "philox.cuh"],
-    "pair_scores": ["select.cu", "pair_math.cuh", "gemm_splitk.cuh", "tcgen05.cuh", "common.cuh"],
+    "pair_scores": ["select.cu", "pair_math.cuh", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
     "proj": ["proj.cu", "pair_math.cuh", "tcgen05.cuh", "common.cuh"],
     "walk": ["walk.cu", "common.cuh", "philox.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
@@ -247,6 +247,7 @@ class Cycle:
         self.target = None
         self.vws = torch.empty(api.verify_workspace(h, nb, L, V), dtype=torch.uint8, device=dev)
         self.cws = torch.empty(api.conv2tap_workspace(h, nb, L, D), dtype=torch.uint8, device=dev)
+        self.pws = torch.empty(api.pair_scores_workspace(h, nb, L, D), dtype=torch.uint8, device=dev)
         # conv x10, top-16, gate + pairs, then per temperature: walk + verify (init + one cooperative kernel)
         self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 2)
 
@@ -260,7 +261,8 @@ class Cycle:
         api.topk(h, self.U, vals=self.vals, idx=self.idx)
         rec("topk")
         ci, cv = self.idx.view(self.nb, L, K), self.vals.view(self.nb, L, K)
-        api.pair_scores(h, ci, cv, self.lv, cur, self.W_H, None, self.A, self.Bt, gate=self.gate, S=self.S)
+        api.pair_scores(h, ci, cv, self.lv, cur, self.W_H, None, self.A, self.Bt, gate=self.gate, S=self.S,
+                        workspace=self.pws)
         rec("pairs")
         for i, T in enumerate((0.0, 1.0)):
             api.walk(h, self.S, ci, temperature=T, seed=1, offset=seed_offset, draft_tok=self.tok[i],

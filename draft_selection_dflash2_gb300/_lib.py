@@ -28,7 +28,8 @@ SIGNATURES = {
     "dflash2_num_sms": (I32, [P]),
     "dflash2_get_device_error": (I32, [P, P, U32P, I32]),
     "dflash2_topk": (I32, [P, P, I64, I64, I64, I32, P, P, P]),
-    "dflash2_pair_scores": (I32, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, P, P]),
+    "dflash2_pair_scores_workspace": (SZ, [P, I64, I64, I64]),
+    "dflash2_pair_scores": (I32, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, P, P, P, SZ, P]),
     "dflash2_walk": (I32, [P, P, P, I64, I64, F32, U64, U64, P, P, P, P]),
     "dflash2_walk_viterbi": (I32, [P, P, P, I64, I64, P, P, P, P]),
     "dflash2_selector_eval": (I32, [P, P, P, I64, I64, P, P, P, P]),

@@ -113,9 +113,16 @@ def topk(h: Handle, logits, V: int = None, vals=None, idx=None, k: int = K, stre
     return vals, idx
 
 
+def pair_scores_workspace(h: Handle, B: int, L: int, d: int) -> int:
+    return int(h._lib.dflash2_pair_scores_workspace(h.ptr, B, L, d))
+
+
 def pair_scores(h: Handle, cand_idx, cand_val, last_verified, hs, W_H, b_H, A, Bt, V: int = None,
-                gate=None, S=None, stream=None):
-    """-> (S fp32 [B, L, 16, 16], gate fp32 [B, L, 256])."""
+                gate=None, S=None, workspace=None, stream=None):
+    """-> (S fp32 [B, L, 16, 16], gate fp32 [B, L, 256]).
+
+    workspace: device bytes (uint8 tensor) of at least pair_scores_workspace(h, B, L, d);
+    allocated here by torch when None."""
     B, L, k = cand_idx.shape
     _need(k == K, "cand_idx: [B, L, 16]")
     d = hs.shape[-1]
@@ -125,9 +132,13 @@ def pair_scores(h: Handle, cand_idx, cand_val, last_verified, hs, W_H, b_H, A, B
         _need(_is16(t) and t.is_contiguous(), f"{name}: contiguous bf16")
     gate = torch.empty((B, L, EMBED), dtype=torch.float32, device=dev) if gate is None else gate
     S = torch.empty((B, L, K, K), dtype=torch.float32, device=dev) if S is None else S
+    if workspace is None:
+        workspace = torch.empty(max(pair_scores_workspace(h, B, L, d), 256), dtype=torch.uint8, device=dev)
     _check(h._lib.dflash2_pair_scores(h.ptr, _ptr(cand_idx), _ptr(cand_val), _ptr(last_verified),
                                       _ptr(hs), _ptr(W_H), _ptr(b_H), _ptr(A), _ptr(Bt), B, L, d, V,
-                                      _ptr(gate), _ptr(S), _stream(stream)), "dflash2_pair_scores")
+                                      _ptr(gate), _ptr(S), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dflash2_pair_scores")
     return S, gate
 
 

@@ -142,10 +142,16 @@ int dflash2_topk(dflash2_handle* h, const uint16_t* logits, int64_t rows, int64_
   return DFLASH2_OK;
 }
 
+size_t dflash2_pair_scores_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d) {
+  if (bad_handle(h) || B <= 0 || L <= 0 || d <= 0 || d % 64 != 0) return 0;
+  return dflash2::gate_workspace_bytes(B, L, d, h->num_sms);
+}
+
 int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float* cand_val,
                         const int32_t* last_verified, const uint16_t* hs, const uint16_t* W_H,
                         const float* b_H, const uint16_t* A, const uint16_t* Bt, int64_t B,
-                        int64_t L, int64_t d, int64_t V, float* gate, float* S, void* stream) {
+                        int64_t L, int64_t d, int64_t V, float* gate, float* S, void* workspace,
+                        size_t ws_bytes, void* stream) {
   const NvtxRange range("dflash2_pair_scores");
   if (bad_handle(h) || B < 0 || L < 0 || d <= 0 || V <= 0) return DFLASH2_ERR_INVALID_ARG;
   if (L > kMaxL || d % 64 != 0 || V >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
@@ -154,14 +160,16 @@ int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float*
     return DFLASH2_ERR_INVALID_ARG;
   if (!aligned(hs, 16) || !aligned(W_H, 16) || !aligned(A, 16) || !aligned(Bt, 16) ||
       !aligned(gate, 16) || !aligned(S, 16) || !aligned(cand_idx, 4) || !aligned(cand_val, 4) ||
-      !aligned(last_verified, 4) || (b_H && !aligned(b_H, 4)))
+      !aligned(last_verified, 4) || (b_H && !aligned(b_H, 4)) || (workspace && !aligned(workspace, 256)))
     return DFLASH2_ERR_MISALIGNED;
+  if (workspace == nullptr || ws_bytes < dflash2::gate_workspace_bytes(B, L, d, h->num_sms))
+    return DFLASH2_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   if (const int st = wrong_device(h)) return st;
-  const int st = launched(dflash2::launch_gate(hs, W_H, b_H, B * L, d, gate, h->err, h->num_sms, s));
+  const int st = launched(dflash2::launch_gate(hs, W_H, b_H, B * L, d, gate, workspace, h->err, h->num_sms, s));
   if (st != DFLASH2_OK) return st;
-  return launched(dflash2::launch_pair_scores(cand_idx, cand_val, last_verified, gate, A, Bt, B, L, V,
-                                              S, h->err, h->num_sms, s));
+  return launched(dflash2::launch_pair_scores(cand_idx, cand_val, last_verified, static_cast<const float*>(workspace),
+                                              b_H, gate, d, A, Bt, B, L, V, S, h->err, h->num_sms, s));
 }
 
 int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,

@@ -57,12 +57,17 @@ int topk_cluster_size(int64_t rows, int64_t V, int num_sms);
 cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, float* vals,
                         int32_t* idx, uint32_t* err, int num_sms, cudaStream_t stream);
 
+// The gate contraction's split-K partials ([ks, B*L, 256] fp32) go to the
+// workspace (the pair kernel turns them into H).
+size_t gate_workspace_bytes(int64_t B, int64_t L, int64_t d, int num_sms);
 cudaError_t launch_gate(const uint16_t* hs, const uint16_t* W_H, const float* b_H, int64_t M,
-                        int64_t d, float* gate, uint32_t* err, int num_sms, cudaStream_t stream);
+                        int64_t d, float* gate, void* workspace, uint32_t* err, int num_sms, cudaStream_t stream);
+// The pair scores; the gate H is formed here from the gate GEMM's partials
+// (gate_part, as launch_gate left them) and written to `gate`.
 cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
-                               const int32_t* last_verified, const float* gate, const uint16_t* A,
-                               const uint16_t* Bt, int64_t B, int64_t L, int64_t V, float* S,
-                               uint32_t* err, int num_sms, cudaStream_t stream);
+                               const int32_t* last_verified, const float* gate_part, const float* b_H, float* gate,
+                               int64_t d, const uint16_t* A, const uint16_t* Bt, int64_t B, int64_t L, int64_t V,
+                               float* S, uint32_t* err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_walk(const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                         float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,

@@ -127,14 +127,22 @@ int dflash2_topk(dflash2_handle* h, const uint16_t* logits, int64_t rows, int64_
  *   hs                  device bf16 [B, L, d] drafter hidden states
  *   W_H                 device bf16 [256, d];  b_H device fp32 [256] or NULL (= 0)
  *   A, Bt               device bf16 [V, 256] predecessor / candidate embeddings
- *   gate                device fp32 [B, L, 256] output: H (also the GEMM result)
+ *   gate                device fp32 [B, L, 256] output: H
  *   S                   device fp32 [B, L, 16, 16] output
- * d % 64 == 0, L <= 64.  Ids outside [0, V) are clamped and flagged.
+ *   workspace           device scratch of at least dflash2_pair_scores_workspace(h, B,
+ *                       L, d) bytes, 256-byte aligned: the gate contraction's fp32
+ *                       split-K partials, rewritten by every call; calls that overlap
+ *                       on the GPU must not share it.  The partials are summed in a
+ *                       fixed order, so H has the same bits on every call.
+ * d % 64 == 0, L <= 64.  Ids outside [0, V) are clamped and flagged.  A too-small
+ * or NULL workspace returns DFLASH2_ERR_WORKSPACE.
  */
+size_t dflash2_pair_scores_workspace(const dflash2_handle* h, int64_t B, int64_t L, int64_t d);
 int dflash2_pair_scores(dflash2_handle* h, const int32_t* cand_idx, const float* cand_val,
                         const int32_t* last_verified, const uint16_t* hs, const uint16_t* W_H,
                         const float* b_H, const uint16_t* A, const uint16_t* Bt, int64_t B,
-                        int64_t L, int64_t d, int64_t V, float* gate, float* S, void* stream);
+                        int64_t L, int64_t d, int64_t V, float* gate, float* S, void* workspace,
+                        size_t ws_bytes, void* stream);
 
 /*
  * Pair scores in projection form.  The score equation of "A Lightweight Path

@@ -42,7 +42,7 @@ def test_null_handle_is_rejected_without_a_device(lib):
     assert lib.dflash2_conv2tap(null, one, one, null, one, one, one, null, 1, 4, 64, one, 1, one, 1 << 20,
                                 null) == -1
     assert lib.dflash2_pair_scores(null, one, one, one, one, one, null, one, one, 1, 4, 64, 64, one,
-                                   one, null) == -1
+                                   one, one, 1 << 20, null) == -1
     assert lib.dflash2_lmhead_topk(null, one, one, 4, 64, 64, one, one, one, 256, null) == -1
     assert lib.dflash2_create(0, None) == -1
 
@@ -53,6 +53,7 @@ def test_workspace_queries_are_host_only(lib):
     assert lib.dflash2_verify_workspace(null, 128, 16, 151936) == 0
     assert lib.dflash2_gemm_conv2tap_workspace(null, 128, 16, 5120) == 0
     assert lib.dflash2_conv2tap_workspace(null, 128, 16, 5120) == 0
+    assert lib.dflash2_pair_scores_workspace(null, 128, 16, 5120) == 0
 
 
 def test_handle_allocates_only_its_error_word():
