@@ -11,7 +11,8 @@ inputs resident in HBM; `e2e` is the same metric through the public API with
 host (pinned) buffers, host<->device copies inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dflash2|reference]
-                  [--no-sweep] [--no-e2e] [--no-cpu-baseline]
+                  [--no-sweep] [--no-e2e] [--no-cpu-baseline] [--no-lmhead] [--no-next]
+                  [--no-small]
 
 --impl reference times the CPU oracle (fp64, all host cores) on a bounded
 sample of the same workload instead.
@@ -248,8 +249,9 @@ class Cycle:
         self.vws = torch.empty(api.verify_workspace(h, nb, L, V), dtype=torch.uint8, device=dev)
         self.cws = torch.empty(api.conv2tap_workspace(h, nb, L, D), dtype=torch.uint8, device=dev)
         self.pws = torch.empty(api.pair_scores_workspace(h, nb, L, D), dtype=torch.uint8, device=dev)
-        # conv x10, top-16, gate + pairs, then per temperature: walk + verify (init + one cooperative kernel)
-        self.launches_per_step = CONV_APPS + 1 + 2 + 2 * (1 + 2)
+        # conv x10 (pair GEMM + tap kernel each), top-16, gate GEMM + pair kernel, walk and verify at T=0
+        # (init + greedy kernel) and T=1 (init + rows kernel + draw kernel)
+        self.launches_per_step = 2 * CONV_APPS + 1 + 2 + (1 + 2) + (1 + 3)
 
     def step(self, ev=None, seed_offset=0):
         api, h = self.api, self.h
@@ -364,10 +366,10 @@ def run_gpu(args):
                      "frac_hbm": round(gbs / hbm, 4)}
     stages["conv"]["per_application_ms"] = round(stage_ms["conv"] / CONV_APPS, 4)
     dom = max(STAGES, key=lambda n: stage_ms[n])
-    kernel_name = {"conv": "splitk_gemm_kernel<ConvEpi>", "topk": "topk16_kernel",
-                   "pairs": "splitk_gemm_kernel<GateEpi> + pair_kernel",
-                   "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_kernel",
-                   "verify1": "verify_kernel"}[dom]
+    kernel_name = {"conv": "pair_gemm_kernel<ConvShape> + conv_tap_kernel", "topk": "topk16_kernel",
+                   "pairs": "pair_gemm_kernel<GateShape> + pair_kernel",
+                   "walk0": "walk_kernel", "walk1": "walk_kernel", "verify0": "verify_greedy_kernel",
+                   "verify1": "verify_rows_kernel + verify_draw_kernel"}[dom]
     per_launch_ms = stage_ms[dom] / (CONV_APPS if dom == "conv" else 1)
     per_launch_bytes = stage_bytes[dom] / (CONV_APPS if dom == "conv" else 1)
     achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
@@ -398,6 +400,9 @@ def run_gpu(args):
 
     if rank == 0 and args.sweep:
         line["sweep"] = run_sweep(torch, api, h, w, cyc, dev, pk)
+        line["sweep_zipf"] = run_sweep(torch, api, h, w, cyc, dev, pk, logits="zipf")
+    if rank == 0 and args.small:
+        line["small_cycles"] = run_small_cycles(torch, api, h, dev)
     if rank == 0 and args.e2e:
         line["e2e"] = run_e2e(torch, api, h, w, cyc, dev, args)
     if rank == 0 and args.lmhead:
@@ -406,7 +411,7 @@ def run_gpu(args):
         line["next"] = run_next(torch, api, h, cyc, dev, pk)
         line["next"]["projection_selector"]["table_form_pairs_ms_in_step"] = stages["pairs"]["ms"]
     if rank == 0 and args.cpu_baseline and world == 1:
-        line["cpu_baseline"] = run_cpu_baseline(w, cyc, tgt, sample=64)
+        line["cpu_baseline"] = run_cpu_baseline(w, tgt)
     if rank == 0:
         print(json.dumps(line), flush=True)
     h.close()
@@ -414,13 +419,31 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_sweep(torch, api, h, w, cyc, dev, pk):
-    """Batch sweep at d=5120: top-16 + pair scores + greedy walk, blocks/s and GB/s per stage."""
+def _zipf_logits_dev(torch, rows, dev, seed=41):
+    """Zipf(1.1)-ranked logits drawn on the device with the same recipe as
+    synth.logits_zipf (N(0, 2^2) + a shared -1.1 ln(1 + rank) bias), bf16 [rows, V]."""
+    bias = torch.from_numpy(synth.zipf_bias(np.random.default_rng(seed), V)).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    U = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, rows, 512):
+        r1 = min(rows, r0 + 512)
+        U[r0:r1] = (torch.randn((r1 - r0, V), generator=g, device=dev) * 2.0 + bias).to(torch.bfloat16)
+    return U
+
+
+def run_sweep(torch, api, h, w, cyc, dev, pk, logits="planted"):
+    """Batch sweep at d=5120: top-16 + pair scores + greedy walk, blocks/s and GB/s
+    per stage, on the planted logits or on Zipf(1.1)-ranked ones."""
     out = []
-    Ufull = to_dev(torch, w["U"][: max(SWEEP_B) * L], dev)
+    if logits == "planted":
+        Ufull = to_dev(torch, w["U"][: max(SWEEP_B) * L], dev)
+    else:
+        Ufull = _zipf_logits_dev(torch, max(SWEEP_B) * L, dev)
     hs_all = torch.empty((max(SWEEP_B), L, D), dtype=torch.bfloat16, device=dev)
     hs_all.copy_(cyc.ybuf[1][:1].expand(max(SWEEP_B), L, D))
     lv = torch.zeros((max(SWEEP_B),), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for nb in SWEEP_B:
         U = Ufull[: nb * L]
         vals = torch.empty((nb * L, K), dtype=torch.float32, device=dev)
@@ -429,7 +452,7 @@ def run_sweep(torch, api, h, w, cyc, dev, pk):
         S = torch.empty((nb, L, K, K), dtype=torch.float32, device=dev)
         tok = torch.empty((nb, L), dtype=torch.int32, device=dev)
         slot = torch.empty((nb, L), dtype=torch.int32, device=dev)
-        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        pws = torch.empty(max(api.pair_scores_workspace(h, nb, L, D), 256), dtype=torch.uint8, device=dev)
         times = {"topk": [], "pairs": [], "walk": []}
         steps = 20
         for it in range(steps + 3):
@@ -439,7 +462,7 @@ def run_sweep(torch, api, h, w, cyc, dev, pk):
             api.topk(h, U, vals=vals, idx=idx)
             e[1].record()
             api.pair_scores(h, idx.view(nb, L, K), vals.view(nb, L, K), lv[:nb], hs_all[:nb], cyc.W_H, None,
-                            cyc.A, cyc.Bt, gate=gate, S=S)
+                            cyc.A, cyc.Bt, gate=gate, S=S, workspace=pws)
             e[2].record()
             api.walk(h, S, idx.view(nb, L, K), draft_tok=tok, draft_slot=slot, want_q=False)
             e[3].record()
@@ -448,15 +471,119 @@ def run_sweep(torch, api, h, w, cyc, dev, pk):
                 times["topk"].append(e[0].elapsed_time(e[1]))
                 times["pairs"].append(e[1].elapsed_time(e[2]))
                 times["walk"].append(e[2].elapsed_time(e[3]))
-        del flush
         med = {k: statistics.median(v) for k, v in times.items()}
         tot = sum(med.values())
-        out.append({"B": nb, "blocks_per_s": round(nb / (tot * 1e-3), 1), "ms": round(tot, 4),
+        out.append({"B": nb, "logits": "planted N(0,1)+4" if logits == "planted" else "zipf(1.1) N(0,4)+bias",
+                    "blocks_per_s": round(nb / (tot * 1e-3), 1), "ms": round(tot, 4),
                     "pair_scores_per_s": round(nb * PAIRS_PER_BLOCK / (med["pairs"] * 1e-3), 1),
                     "topk_GBps": round(bytes_topk(nb) / (med["topk"] * 1e-3) / 1e9, 1),
                     "pairs_GBps": round(bytes_pairs(nb) / (med["pairs"] * 1e-3) / 1e9, 1),
                     "topk_frac_hbm": round(bytes_topk(nb) / (med["topk"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                    "pairs_frac_hbm": round(bytes_pairs(nb) / (med["pairs"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                     "walk_us": round(med["walk"] * 1e3, 2)})
+    del flush, Ufull
+    return out
+
+
+def _small_inputs(torch, wl, dev):
+    """Device inputs of one cycle of a small workload (seeded, synth recipes)."""
+    si = synth.selector_inputs(31, wl.B, wl.L, wl.V, wl.d, logits=wl.logits)
+    bf = lambda a: to_dev(torch, a, dev)  # noqa: E731
+    t = {"U": bf(si.U.reshape(wl.B * wl.L, wl.V)), "W_H": bf(si.W_H), "A": bf(si.A), "Bt": bf(si.Bt),
+         "lv": to_dev(torch, si.last_verified, dev)}
+    if wl.conv_apps:
+        c = synth.conv_inputs(32, wl.B, wl.L, wl.d)
+        t.update(x=bf(c.x), xp=bf(c.x_prev), k0=bf(c.k0), k1=bf(c.k1), W_c=bf(c.W_c))
+    else:
+        t["hs"] = bf(si.h)
+    return t
+
+
+def run_small_cycles(torch, api, h, dev):
+    """Microseconds per cycle at B=1 for the tiny selector (L=8, V=4096, d=512:
+    top-16, gate + pair scores, walk T=0) and the Qwen3-4B-shaped head (L=16,
+    V=151936, d=2560, Zipf logits: conv, top-16, gate + pair scores, walk T=0
+    and T=1).  Each cycle is replayed from a CUDA graph, cycles back to back on
+    one stream.  Hot L2: the same inputs every cycle.  Cold L2: the graph
+    rotates through copies of all inputs and parameters whose bytes read per
+    cycle add up to at least four times the L2 between two uses of a copy."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for key, wl in (("tiny_selector", synth.TINY_SELECTOR), ("qwen3_4b_head", synth.QWEN3_4B_HEAD)):
+        nb, Lw, d = wl.B, wl.L, wl.d
+        base = _small_inputs(torch, wl, dev)
+        read = nb * Lw * wl.V * 2 + nb * Lw * d * 2 + R * d * 2 + nb * ((K * (Lw - 1) + 1) + K * Lw) * R * 2
+        if wl.conv_apps:
+            read += nb * d * 2 + 2 * (d // 16) * d * 2 + 2 * d * 2
+        n_copies = int(min(2048, max(2, -(-4 * l2 // read))))
+        copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+        vals = torch.empty((nb * Lw, K), dtype=torch.float32, device=dev)
+        idx = torch.empty((nb * Lw, K), dtype=torch.int32, device=dev)
+        hs = torch.empty((nb, Lw, d), dtype=torch.bfloat16, device=dev)
+        gate = torch.empty((nb, Lw, R), dtype=torch.float32, device=dev)
+        S = torch.empty((nb, Lw, K, K), dtype=torch.float32, device=dev)
+        nT = len(wl.temperatures)
+        tok = [torch.empty((nb, Lw), dtype=torch.int32, device=dev) for _ in range(nT)]
+        slot = [torch.empty((nb, Lw), dtype=torch.int32, device=dev) for _ in range(nT)]
+        q = [torch.empty((nb, Lw, K), dtype=torch.float32, device=dev) for _ in range(nT)]
+        cws = torch.empty(max(api.conv2tap_workspace(h, nb, Lw, d), 256), dtype=torch.uint8, device=dev)
+        pws = torch.empty(max(api.pair_scores_workspace(h, nb, Lw, d), 256), dtype=torch.uint8, device=dev)
+        launches = (2 if wl.conv_apps else 0) + 1 + 2 + nT
+
+        def cycle(c):
+            cur = c["hs"] if "hs" in c else api.conv2tap(h, c["x"], c["xp"], c["k0"], c["k1"], c["W_c"], y=hs,
+                                                         workspace=cws)
+            api.topk(h, c["U"], vals=vals, idx=idx)
+            ci, cv = idx.view(nb, Lw, K), vals.view(nb, Lw, K)
+            api.pair_scores(h, ci, cv, c["lv"], cur, c["W_H"], None, c["A"], c["Bt"], gate=gate, S=S, workspace=pws)
+            for i, T in enumerate(wl.temperatures):
+                api.walk(h, S, ci, temperature=T, seed=1, draft_tok=tok[i], draft_slot=slot[i], draft_q=q[i])
+
+        for c in copies:
+            cycle(c)
+        torch.cuda.synchronize()
+        # eager launches from Python (host launch overhead included), hot inputs
+        eager_n = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(eager_n):
+            cycle(copies[0])
+        e1.record()
+        torch.cuda.synchronize()
+        eager_us = e0.elapsed_time(e1) * 1e3 / eager_n
+        hot_n = 64
+        g_hot, g_cold = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_hot):
+            for _ in range(hot_n):
+                cycle(copies[0])
+        with torch.cuda.graph(g_cold):
+            for c in copies:
+                cycle(c)
+
+        def per_cycle_us(g, n_cycles, reps):
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / (reps * n_cycles)
+
+        hot_us = per_cycle_us(g_hot, hot_n, 20)
+        cold_us = per_cycle_us(g_cold, n_copies, max(2, 2048 // n_copies))
+        assert h.device_error() == 0, f"device error in the {key} cycles"
+        out[key] = {"workload": wl.name + ", " + ", ".join(
+                        (["conv x1"] if wl.conv_apps else []) + ["top-16", "gate + pair scores"]
+                        + [f"walk T={T:g}" for T in wl.temperatures]),
+                    "us_per_cycle_hot_l2": round(hot_us, 2), "us_per_cycle_cold_l2": round(cold_us, 2),
+                    "us_per_cycle_eager_launch_hot_l2": round(eager_us, 2),
+                    "kernel_launches_per_cycle": launches,
+                    "cold_l2": f"{n_copies} rotating copies of every input and parameter, "
+                               f"{read} bytes read per cycle ({n_copies * read / l2:.1f}x L2 between reuses)",
+                    "timing": "CUDA graph replay, cycles back to back on one stream, CUDA events"}
+        del g_hot, g_cold, copies, base
     return out
 
 
@@ -766,15 +893,69 @@ def oracle_cycle(w, target_bits, nb, nthreads):
     return accs
 
 
-def run_cpu_baseline(w, cyc, target_bits, sample=8):
+def cpu_info():
+    """CPU model (lscpu, else /proc/cpuinfo), logical CPUs and the CPUs this process may use."""
+    model = None
+    try:
+        txt = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in txt.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    return {"model": model, "logical_cpus": os.cpu_count(), "usable_cpus": len(os.sched_getaffinity(0))}
+
+
+def _repeat(fn, repeats):
+    ts = []
+    for _ in range(repeats):
+        t = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t)
+    return ts
+
+
+def run_cpu_baseline(w, target_bits, sample_all=64, sample_one=4, repeats=3, lm_rows_all=16, lm_rows_one=1):
+    """The oracle as it stands on the host cores: the full cycle on a sample of the
+    workload's sequences, all cores and one thread, several repeats each; and the
+    LM head + top-16 oracle's time per row on the C4 shapes (d=5120, V=151936)."""
     import oracle
     threads = oracle.default_threads()
     used = oracle.threads_used(threads)
-    t = time.perf_counter()
-    oracle_cycle(w, target_bits, sample, threads)
-    dt = time.perf_counter() - t
-    return {"value": round(sample / dt, 4), "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"first {sample} of {B} sequences of the workload, one full cycle ({dt:.1f} s)"}
+    t_all = _repeat(lambda: oracle_cycle(w, target_bits, sample_all, threads), repeats)
+    t_one = _repeat(lambda: oracle_cycle(w, target_bits, sample_one, 1), repeats)
+    med_all, med_one = statistics.median(t_all), statistics.median(t_one)
+    # C4: W is a seeded N(0, 0.02^2) block of 4096 rows tiled to V rows (drawing all
+    # 778M values would take longer than the timing; the oracle's cost does not
+    # depend on the values)
+    block = synth.normal_bits(4, (4096, D), std=0.02)
+    W = np.tile(block, (-(-V // 4096), 1))[:V]
+    hidden = synth.normal_bits(5, (lm_rows_all, D))
+    lm_all = _repeat(lambda: oracle.lmhead_topk(hidden, W, np.arange(lm_rows_all), nthreads=threads), repeats)
+    lm_one = _repeat(lambda: oracle.lmhead_topk(hidden, W, np.arange(lm_rows_one), nthreads=1), repeats)
+    del W
+    return {"value": round(sample_all / med_all, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"first {sample_all} of {B} sequences of the workload, one full cycle, median of "
+                      f"{repeats} repeats on {used} threads",
+            "cpu": cpu_info(),
+            "all_cores": {"threads": used, "sequences": sample_all, "seconds": [round(t, 3) for t in t_all],
+                          "blocks_per_s": round(sample_all / med_all, 4)},
+            "single_thread": {"threads": 1, "sequences": sample_one, "seconds": [round(t, 3) for t in t_one],
+                              "blocks_per_s": round(sample_one / med_one, 4)},
+            "lmhead_topk_per_row": {
+                "workload": f"fused LM-head top-16 rows, d={D} V={V} (fp64 dot products)",
+                "all_cores_s_per_row": round(statistics.median(lm_all) / lm_rows_all, 4),
+                "all_cores_rows": lm_rows_all,
+                "single_thread_s_per_row": round(statistics.median(lm_one) / lm_rows_one, 4),
+                "single_thread_rows": lm_rows_one, "repeats": repeats,
+                "M1024_extrapolated_s_all_cores": round(1024 * statistics.median(lm_all) / lm_rows_all, 1)}}
 
 
 def run_reference(args):
@@ -802,7 +983,11 @@ def run_reference(args):
             "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": WORKLOAD, "B": B, "L": L, "V": V, "d": D,
-                       "sample_sequences_per_step": sample},
+                       "sample_sequences_per_step": sample,
+                       "target": "planted (0.85 agreement) on seeded random tokens, not on the oracle's own "
+                                 "draft, so acceptance lengths differ from the GPU arm's; the cost per cycle "
+                                 "is that of the same stages at the same shapes"},
+            "cpu": cpu_info(),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": used, "kind": "oracle",
                              "sample": f"{sample} of {B} sequences per step, full cycle"},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -820,6 +1005,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-lmhead", dest="lmhead", action="store_false")
     ap.add_argument("--no-next", dest="next", action="store_false")
+    ap.add_argument("--no-small", dest="small", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

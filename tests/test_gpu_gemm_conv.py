@@ -1,6 +1,6 @@
 """The two-tap conv fused into its producing GEMM, on the GPU, against the
-oracle (fp32 accumulation over K products: 1e-3 rel / 1e-3 abs on fp32 output,
-one bf16 ulp on bf16 output), and bit for bit against the unfused path (the
+oracle (fp32 accumulation over K products: 1e-3 rel / 1e-4 abs on fp32 output,
+one bf16 ulp + 1e-4 abs on bf16 output), and bit for bit against the unfused path (the
 conv kernel on an exact x) where the GEMM output is exact."""
 import numpy as np
 import pytest
@@ -36,7 +36,7 @@ def test_fused_conv_matches_oracle(handle, B, L, K, d, bias):
     y, cw = run(handle, c, A, W, h)
     assert handle.device_error() == 0
     oy = oracle.gemm_conv2tap(A, W, c.x_prev, h, c.k0, c.k1, c.W_c, b_c=c.b_c)
-    assert_close(y, oy, rtol=1e-3, atol=1e-3, what="y")
+    assert_close(y, oy, rtol=1e-3, atol=1e-4, what="y")
 
 
 def bf16_ulp(v):
@@ -49,7 +49,7 @@ def test_fused_conv_bf16_within_one_ulp(handle):
     y, _ = run(handle, c, A, W, h, y_fp32=False)
     oy = oracle.gemm_conv2tap(A, W, c.x_prev, h, c.k0, c.k1, c.W_c)
     got = synth.bf16_to_f32(y).astype(np.float64)
-    assert np.all(np.abs(got - oy) <= bf16_ulp(oy) + 1e-3)
+    assert np.all(np.abs(got - oy) <= bf16_ulp(oy) + 1e-4)
 
 
 def exact_case(seed, B, L, K, d):
