@@ -189,13 +189,11 @@ int dflash2_pair_scores_proj(dflash2_handle* h, const int32_t* cand_idx, const f
  *     seed_hi), u = (x0 >> 8) * 2^-24; slot = smallest j with
  *     u Z < w_0 + ... + w_j; draft_q[b,t,j] = w_j / Z.  A row with no positive
  *     weight (every score NaN or -inf) takes the greedy slot, q one-hot there.
- *   S          device fp32 [B, L, 16, 16], 16-byte aligned (each sequence's
- *              block is staged in shared memory by one bulk copy)
+ *   S          device fp32 [B, L, 16, 16], 16-byte aligned (read with 16-byte loads)
  *   cand_idx   device int32 [B, L, 16]
  *   draft_tok  device int32 [B, L];  draft_slot device int32 [B, L]
  *   draft_q    device fp32 [B, L, 16] or NULL
- * A staging copy that does not complete within the wait limit raises
- * DFLASH2_DEVERR_TIMEOUT and leaves that sequence's outputs unwritten.
+ * Nothing in the walk waits on the device; draft_tok takes cand_idx as stored.
  */
 int dflash2_walk(dflash2_handle* h, const float* S, const int32_t* cand_idx, int64_t B, int64_t L,
                  float temperature, uint64_t seed, uint64_t offset, int32_t* draft_tok,
