@@ -262,17 +262,86 @@ __device__ __forceinline__ void fixed_weight_parts(float l, const WeightParams& 
   Bs += __float_as_uint(t2);
 }
 
+// Packed fp32 pairs (Blackwell's f32x2 arithmetic: two independent fp32
+// operations per instruction, each rounded exactly as the scalar operation
+// with the same rounding mode).  Element 0 of a pair sits in the low 32 bits.
+struct F2 {
+  uint64_t v;
+  __device__ __forceinline__ float lo() const { return __uint_as_float(static_cast<uint32_t>(v)); }
+  __device__ __forceinline__ float hi() const { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+  return {static_cast<uint64_t>(__float_as_uint(hi)) << 32 | __float_as_uint(lo)};
+}
+__device__ __forceinline__ F2 f2_add_rn(F2 a, F2 b) {
+  F2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+  return d;
+}
+__device__ __forceinline__ F2 f2_sub_rn(F2 a, F2 b) {
+  F2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+  return d;
+}
+__device__ __forceinline__ F2 f2_mul_rn(F2 a, F2 b) {
+  F2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+  return d;
+}
+__device__ __forceinline__ F2 f2_fma_rn(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return d;
+}
+__device__ __forceinline__ F2 f2_add_rz(F2 a, F2 b) {
+  F2 d;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+  return d;
+}
+__device__ __forceinline__ F2 f2_fma_rz(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("fma.rz.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return d;
+}
+
+// fixed_weight_parts on two logits at once: the same operations in the same
+// order, two lanes per instruction (the clamp and the integer steps per lane).
+__device__ __forceinline__ void fixed_weight_parts2(F2 l, F2 Mp, F2 cp, uint32_t& A, uint32_t& Bs) {
+  F2 x = f2_mul_rn(f2_sub_rn(l, Mp), cp);
+  x = f2(fmaxf(x.lo(), -60.0f), fmaxf(x.hi(), -60.0f));
+  const F2 K = f2(12582912.0f, 12582912.0f);
+  const F2 t = f2_add_rn(x, K);
+  const F2 f = f2_sub_rn(x, f2_sub_rn(t, K));
+  F2 p = f2(1.525273365e-05f, 1.525273365e-05f);
+  p = f2_fma_rn(p, f, f2(1.540352969e-04f, 1.540352969e-04f));
+  p = f2_fma_rn(p, f, f2(1.333355787e-03f, 1.333355787e-03f));
+  p = f2_fma_rn(p, f, f2(9.618128650e-03f, 9.618128650e-03f));
+  p = f2_fma_rn(p, f, f2(5.550410971e-02f, 5.550410971e-02f));
+  p = f2_fma_rn(p, f, f2(2.402265072e-01f, 2.402265072e-01f));
+  p = f2_fma_rn(p, f, f2(6.931471825e-01f, 6.931471825e-01f));
+  p = f2_fma_rn(p, f, f2(1.0f, 1.0f));
+  const F2 sc = f2(__uint_as_float((__float_as_uint(t.lo()) << 23) + (144u << 23)),
+                   __uint_as_float((__float_as_uint(t.hi()) << 23) + (144u << 23)));
+  const F2 yp = f2_mul_rn(p, sc);
+  const F2 two23 = f2(8388608.0f, 8388608.0f);
+  const F2 t1 = f2_add_rz(yp, two23);
+  const F2 fr = f2_sub_rn(yp, f2_sub_rn(t1, two23));
+  const F2 t2 = f2_fma_rz(fr, two23, two23);
+  A += __float_as_uint(t1.lo()) + __float_as_uint(t1.hi());
+  Bs += __float_as_uint(t2.lo()) + __float_as_uint(t2.hi());
+}
+
 // The weights of the 8 logits of a 16-byte vector, summed.  Each sum of 8 a's
 // (< 2^21) and 8 b's (< 2^26) is taken modulo 2^32 with the 8 biases removed
 // at the end, which is exact because the true sums fit.
 __device__ __forceinline__ uint64_t vec_weight(const uint4& v, const WeightParams& wp) {
   uint32_t A = 0u, Bs = 0u;
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const F2 Mp = f2(wp.M, wp.M), cp = f2(wp.c, wp.c);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    fixed_weight_parts(__uint_as_float(w[k] << 16), wp, A, Bs);
-    fixed_weight_parts(__uint_as_float(w[k] & 0xFFFF0000u), wp, A, Bs);
-  }
+  for (int k = 0; k < 4; ++k)
+    fixed_weight_parts2({static_cast<uint64_t>(w[k] & 0xFFFF0000u) << 32 | static_cast<uint64_t>(w[k] << 16)}, Mp,
+                        cp, A, Bs);
   A -= 8u * 0x4B000000u;
   Bs -= 8u * 0x4B000000u;
   return (static_cast<uint64_t>(A) << 23) + Bs;
