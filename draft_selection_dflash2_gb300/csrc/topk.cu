@@ -389,17 +389,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
   }
   uint32_t lane_max = 0u;   // the largest of this thread's group entries
   for (int it = 0; it < iters; ++it) {
-    uint32_t w2[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) w2[u] = max2_bits(max2_bits(v[u].x, v[u].y), max2_bits(v[u].z, v[u].w));
     const int64_t nb = static_cast<int64_t>(it + 1) * per_iter;
+    uint32_t m2 = 0u;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t w = max2_bits(max2_bits(v[u].x, v[u].y), max2_bits(v[u].z, v[u].w));
+      m2 = u == 0 ? w : max2_bits(m2, w);
       const int64_t vi = nb + u * stride + tid;
       v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : nan4;
     }
-    const uint32_t m2 = max2_bits(max2_bits(max2_bits(w2[0], w2[1]), max2_bits(w2[2], w2[3])),
-                                  max2_bits(max2_bits(w2[4], w2[5]), max2_bits(w2[6], w2[7])));
     const __nv_bfloat162 mb = *reinterpret_cast<const __nv_bfloat162*>(&m2);
     const uint32_t gm = __bfloat16_as_ushort(__hmax(__low2bfloat16(mb), __high2bfloat16(mb)));
     const bool has = static_cast<int64_t>(it) * per_iter + tid < n_vecs;
@@ -536,12 +534,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
 }  // namespace
 
 int topk_cluster_size(int64_t rows, int64_t V, int num_sms) {
-  // Enough CTAs for ~6 resident per SM, never a segment under 8192 logits.
-  const int64_t want = (6LL * num_sms + rows - 1) / rows;
-  int S = 1;
-  while (S < want && S < 16) S <<= 1;
-  while (S > 1 && (V + S - 1) / S < 8192) S >>= 1;
-  return S;
+  // The CTAs run in waves of kCtasPerSm per SM, each wave as long as its
+  // segments.  With rows for at least half the slots, whole rows (a split
+  // costs a cluster merge and wave tails, measured slower at 2048 rows);
+  // otherwise the split S (segments of at least 8192 logits) that minimises
+  // waves x (segment + a fixed cost of about 8192 logits per CTA).
+  const int64_t slots = static_cast<int64_t>(kCtasPerSm) * num_sms;
+  if (2 * rows >= slots) return 1;
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int S = 1; S <= 16; S <<= 1) {
+    if (S > 1 && (V + S - 1) / S < 8192) break;
+    const int64_t waves = (rows * S + slots - 1) / slots;
+    const int64_t cost = waves * ((V + S - 1) / S + 8192);
+    if (best_cost < 0 || cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_topk(const uint16_t* logits, int64_t rows, int64_t V, int64_t ld, float* vals,
