@@ -66,6 +66,7 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowWarpsC = kRowWarps;   // warp runs per slice (the draw reads their sums)
 constexpr int kPieceIds = 20480;     // ids per shared-memory buffer (40 KB; a slice of V <= 163,840 fits one)
 constexpr int kDrawThreads = 256;
+constexpr int kDrawKeep = 2;         // run vectors a draw thread keeps in shared memory
 constexpr float kLog2e = 1.44269504f;   // the walk's constant: the same fp32 value
 
 // Chunks per row (about kChunkIds ids each, at most kMaxChunks) and ids per
@@ -918,7 +919,11 @@ struct DrawSmem {
   uint64_t cand_r[kTopK];       // first slot of an id: its residual weight
   uint64_t cand_d[kTopK];       // first slot of an id: residual - weight (mod 2^64); else 0
   int cand_first[kTopK];
+  uint64_t cand_w[kTopK];       // the candidate's own weight W
+  uint64_t ss[kRowCluster];                 // the row's slice sums (from the rows kernel)
+  uint64_t rs[kRowCluster * kRowWarpsC];    // its warp-run sums
   uint64_t runs[kDrawThreads];  // mass of each thread's run of vectors
+  uint4 keep[kDrawKeep][kDrawThreads];      // each thread's run vectors, when they fit
 };
 
 // Inverse CDF over n <= 256 integer masses mass[0..n) in order (warp 0, 8 per
@@ -982,17 +987,24 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
   const int nc0 = n < L ? kTopK : 0;
   // each candidate slot takes Q_j off its id; the first slot of an id carries
   // the id's residual and its change of mass
+  // (the slice and warp-run sums load meanwhile)
   if (tid < kTopK) {
     int32_t id = 0;
-    uint64_t Q = 0ull;
+    uint64_t Q = 0ull, w = 0ull;
     if (tid < nc0) {
       id = clamp_token(a.cand_idx[(b * L + n) * kTopK + tid], V, a.err);
       const float qj = a.draft_q[(b * L + n) * kTopK + tid];
       const double qc = qj > 0.0f ? fmin(static_cast<double>(qj), 1.0) : 0.0;
       Q = __double2ull_rz(__dmul_rn(qc, __ull2double_rn(Z)));
+      w = fixed_weight1(row[id], wp);
     }
     s.cand[tid] = id;
     s.cand_q[tid] = Q;
+    s.cand_w[tid] = w;
+  } else if (tid >= 32 && tid < 32 + kRowCluster * kRowWarpsC) {
+    s.rs[tid - 32] = __ldcg(rsum + (tid - 32));
+  } else if (tid >= 128 && tid < 128 + kRowCluster) {
+    s.ss[tid - 128] = __ldcg(ssum + (tid - 128));
   }
   __syncthreads();
   if (tid < kTopK) {
@@ -1005,7 +1017,7 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
           qs += s.cand_q[i];
           if (i < tid) first = 0;
         }
-      const uint64_t w = fixed_weight1(row[s.cand[tid]], wp);
+      const uint64_t w = s.cand_w[tid];
       r = w > qs ? w - qs : 0ull;
       dlt = r - w;
     }
@@ -1021,7 +1033,7 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
     int nc = nc0;
     const int k = lane & (kRowCluster - 1);
     const int64_t lo = imin64(k * sl, V), hi = imin64(lo + sl, V);
-    const uint64_t base = __ldcg(ssum + k);
+    const uint64_t base = s.ss[k];
     uint64_t m = base + cand_delta(s, nc, lo, hi);
     uint64_t total = warp_sum_u64(lane < kRowCluster ? m : 0ull);
     if (nc > 0 && total == 0ull) nc = 0;
@@ -1043,7 +1055,7 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
     const int w = lane & (kRowWarps - 1);
     const int64_t r0 = d0 + imin64(w * nvw, nvs) * 8;
     const int64_t r1 = w == kRowWarps - 1 ? d1 : d0 + imin64(imin64(w * nvw, nvs) + nvw, nvs) * 8;
-    const uint64_t rm = __ldcg(rsum + ks * kRowWarps + w) + cand_delta(s, nc, r0, r1);
+    const uint64_t rm = s.rs[ks * kRowWarps + w] + cand_delta(s, nc, r0, r1);
     const uint64_t rincl = warp_scan_u64(lane < kRowWarps ? rm : 0ull, lane);
     const unsigned rhit = __ballot_sync(0xFFFFFFFFu, lane < kRowWarps && t2 < rincl);
     const int rw = rhit ? __ffs(rhit) - 1 : kRowWarps - 1;
@@ -1079,7 +1091,10 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
       for (int k = 0; k < 8; ++k) vv[k] = i + k < i1 ? ldg_stream(rv + i + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (i + k < i1) m += vec_weight(vv[k], wp);
+        if (i + k < i1) {
+          m += vec_weight(vv[k], wp);
+          if (per <= kDrawKeep && k < kDrawKeep) s.keep[k][tid] = vv[k];
+        }
     }
     for (int64_t e = lo + nv * 8; tid == kDrawThreads - 1 && e < hi; ++e) m += fixed_weight1(row[e], wp);
     s.runs[tid] = m;
@@ -1102,7 +1117,9 @@ __device__ int32_t draw_row(DrawSmem& s, const VerifyArgs& a, const uint16_t* ro
       if (v < thi) {
         const int64_t ve = imin64(v + 8, thi);
         if (ve - v == 8) {
-          mv = vec_weight(ldg_stream(reinterpret_cast<const uint4*>(row + v)), wp);
+          // the picked thread's own vectors stayed in shared memory when they fit
+          const int64_t kv = (v - tlo) >> 3;
+          mv = vec_weight(per <= kDrawKeep ? s.keep[kv][th] : ldg_stream(reinterpret_cast<const uint4*>(row + v)), wp);
         } else {
           for (int64_t e = v; e < ve; ++e) mv += fixed_weight1(row[e], wp);
         }
