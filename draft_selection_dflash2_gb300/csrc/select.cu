@@ -6,17 +6,19 @@
 //                  CTA pairs (tcgen05.mma.cta_group::2 + TMA, fp32 in TMEM), the
 //                  K loop split into fp32 partials that a finishing kernel sums
 //                  in a fixed order before the bias and the sigmoid.
-// pair_kernel      persistent, block positions strided over the CTAs: for each
-//                  (b, t) gathers the 16 predecessor rows of A and the 16
-//                  candidate rows of B (512 B each) with 16-byte loads and the
-//                  position's gate partials, forms H_t (and writes it), G =
-//                  A_pred (.) H_t in fp32 shared memory and computes the
-//                  16 x 16 x 256 products (pair_math.cuh); the next position's
-//                  rows and partials are gathered while the products run.
+// pair_kernel      one warp per block position at a time (positions strided
+//                  over all warps of a one-CTA-per-SM grid): the warp copies
+//                  the 16 predecessor rows of A, the 16 candidate rows of B
+//                  (512 B each) and the position's gate partials into its own
+//                  shared memory with 16-byte cp.async, forms H_t (and writes
+//                  it), then takes the 16 x 16 x 256 products on the tensor
+//                  cores (mma.sync m16n8k16, bf16 in, fp32 accumulate): B's rows
+//                  are bf16 already, and G = A_pred (.) H_t in fp32 enters as
+//                  the sum of two bf16 terms, its rounding and the rounding of
+//                  the remainder, which carries G to about 2^-16 of its size.
 #include "common.cuh"
 #include "gemm_pair.cuh"
 #include "launch.h"
-#include "pair_math.cuh"
 
 namespace dflash2 {
 namespace {
@@ -53,148 +55,144 @@ PairGemmShape gate_plan(int64_t M, int64_t d, int num_sms) {
 // ---------------------------------------------------------------------------
 // pair scores
 // ---------------------------------------------------------------------------
-constexpr int kPairCtasPerSm = 3;
+constexpr int kPairWarps = 8;           // warps per CTA, one CTA per SM
+constexpr int kRowPitch = kEmbed + 8;   // bf16 row pitch in shared memory (528 B: ldmatrix rows on distinct banks)
 
-// One position's gathered operands, in registers: thread tid's items are rows
-// tid / 32 + 8 it (it = 0, 1: A rows; 2, 3: B rows), 16-byte chunk tid % 32,
-// plus float4 items tid and tid + 256 of the position's gate partials
-// ([KS][256], split-major).
-template <int KS>
-struct PairStage {
-  static constexpr int kItems = (KS * kEmbed / 4 + 255) / 256;
-  uint4 raw[4];
-  float4 part[kItems];
-};
-
-template <int KS>
-__device__ __forceinline__ void pair_issue(PairStage<KS>& st, const int32_t* ids, const uint16_t* __restrict__ A,
-                                           const uint16_t* __restrict__ Bt, const float* __restrict__ gpart,
-                                           int64_t M, int64_t pos, int tid) {
-  const int ch = tid & 31;
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int row = (tid >> 5) + 8 * it;   // 0..15: A (predecessors), 16..31: B (candidates)
-    const uint16_t* src = row < kTopK ? A + static_cast<int64_t>(ids[row]) * kEmbed
-                                      : Bt + static_cast<int64_t>(ids[row]) * kEmbed;
-    st.raw[it] = *reinterpret_cast<const uint4*>(src + ch * 8);
-  }
-#pragma unroll
-  for (int k = 0; k < PairStage<KS>::kItems; ++k) {
-    const int item = tid + 256 * k;   // split item / 64, float4 item % 64
-    if (item < KS * kEmbed / 4)
-      st.part[k] = __ldcg(reinterpret_cast<const float4*>(gpart + ((item >> 6) * M + pos) * kEmbed) + (item & 63));
-  }
+// one warp's shared memory: A rows, B rows (bf16), the gate partials and H (fp32)
+__host__ __device__ inline size_t pair_warp_bytes(int ks) {
+  return static_cast<size_t>(2 * kTopK * kRowPitch * 2) + static_cast<size_t>(ks) * kEmbed * 4 + kEmbed * 4;
 }
 
-// H_t = sigmoid(sum of the KS partials in split order + b_H) into Hs (shared)
-// and the gate output; whole-CTA call, two barriers.
-template <int KS>
-__device__ __forceinline__ void pair_gate(const PairStage<KS>& st, float* Pb, float* Hs, const float* __restrict__ b_H,
-                                          float* __restrict__ gate, int64_t pos, int tid) {
-#pragma unroll
-  for (int k = 0; k < PairStage<KS>::kItems; ++k) {
-    const int item = tid + 256 * k;
-    if (item < KS * kEmbed / 4) *reinterpret_cast<float4*>(Pb + item * 4) = st.part[k];
-  }
-  __syncthreads();
-  if (tid < kEmbed / 4) {
-    float4 z = *reinterpret_cast<const float4*>(Pb + tid * 4);
-#pragma unroll
-    for (int q = 1; q < KS; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(Pb + q * kEmbed + tid * 4);
-      z.x += v.x;
-      z.y += v.y;
-      z.z += v.z;
-      z.w += v.w;
-    }
-    const float zz[4] = {z.x, z.y, z.z, z.w};
-    float o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = 1.0f / (1.0f + expf(-(zz[j] + (b_H ? b_H[tid * 4 + j] : 0.0f))));
-    const float4 h = make_float4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<float4*>(Hs + tid * 4) = h;
-    *reinterpret_cast<float4*>(gate + pos * kEmbed + tid * 4) = h;
-  }
-  __syncthreads();
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
-// G = A_pred (.) H_t and Bc = B_cand in fp32 shared memory.
-template <int KS>
-__device__ __forceinline__ void pair_store(const PairStage<KS>& st, const float* Hs, float (*G)[kEmbed],
-                                           float (*Bc)[kEmbed], int tid) {
-  const int ch = tid & 31;
-  const float4 h0 = *reinterpret_cast<const float4*>(Hs + ch * 8), h1 = *reinterpret_cast<const float4*>(Hs + ch * 8 + 4);
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int row = (tid >> 5) + 8 * it;
-    const uint32_t w[4] = {st.raw[it].x, st.raw[it].y, st.raw[it].z, st.raw[it].w};
-    float f[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      f[2 * q] = bf16_bits_to_float(w[q] & 0xFFFFu);
-      f[2 * q + 1] = bf16_bits_to_float(w[q] >> 16);
-    }
-    if (row < kTopK) {
-      f[0] *= h0.x; f[1] *= h0.y; f[2] *= h0.z; f[3] *= h0.w;
-      f[4] *= h1.x; f[5] *= h1.y; f[6] *= h1.z; f[7] *= h1.w;
-      *reinterpret_cast<float4*>(&G[row][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(&G[row][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
-    } else {
-      *reinterpret_cast<float4*>(&Bc[row - kTopK][ch * 8]) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(&Bc[row - kTopK][ch * 8 + 4]) = make_float4(f[4], f[5], f[6], f[7]);
-    }
-  }
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
 }
 
-// Persistent: CTA c takes positions c, c + grid, ...  While the products of
-// one position run, the rows and gate partials of the next are in flight in
-// registers and the ids of the one after that are loading.
+// D += A B, m16n8k16, bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two bf16 values (low, high halves of w) times (h0, h1) in fp32, split into
+// the rounded products (hi) and the rounded remainders (lo).
+__device__ __forceinline__ void scale_split(uint32_t w, float h0, float h1, uint32_t& hi, uint32_t& lo) {
+  const float g0 = __uint_as_float(w << 16) * h0, g1 = __uint_as_float(w & 0xFFFF0000u) * h1;
+  const __nv_bfloat162 hb = __floats2bfloat162_rn(g0, g1);
+  const float r0 = g0 - __low2float(hb), r1 = g1 - __high2float(hb);
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(r0, r1);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
+}
+
 template <int KS>
-__global__ void __launch_bounds__(256, kPairCtasPerSm) pair_kernel(const int32_t* __restrict__ cand_idx,
-                                                                   const float* __restrict__ cand_val,
-                                                                   const int32_t* __restrict__ last_verified,
-                                                                   const float* __restrict__ gpart,
-                                                                   const float* __restrict__ b_H,
-                                                                   float* __restrict__ gate,
-                                                                   const uint16_t* __restrict__ A,
-                                                                   const uint16_t* __restrict__ Bt, int64_t L,
-                                                                   int64_t V, int64_t npos, float* __restrict__ S,
-                                                                   uint32_t* __restrict__ err) {
+__global__ void __launch_bounds__(kPairWarps * 32, 1) pair_kernel(const int32_t* __restrict__ cand_idx,
+                                                                 const float* __restrict__ cand_val,
+                                                                 const int32_t* __restrict__ last_verified,
+                                                                 const float* __restrict__ gpart,
+                                                                 const float* __restrict__ b_H,
+                                                                 float* __restrict__ gate,
+                                                                 const uint16_t* __restrict__ A,
+                                                                 const uint16_t* __restrict__ Bt, int64_t L,
+                                                                 int64_t V, int64_t npos, float* __restrict__ S,
+                                                                 uint32_t* __restrict__ err) {
+  extern __shared__ __align__(16) uint8_t pair_smem[];
   pdl_wait();
   pdl_launch_dependents();
-  __shared__ __align__(16) float G[kTopK][kEmbed];    // A[pred_i] (.) H_t
-  __shared__ __align__(16) float Bc[kTopK][kEmbed];   // B[cand_j]
-  __shared__ __align__(16) float Pb[KS * kEmbed];     // the position's gate partials
-  __shared__ __align__(16) float Hs[kEmbed];          // H_t
-  __shared__ int32_t ids[2][2 * kTopK];               // pred (0..15) and cand (16..31) ids of coming positions
-  const int tid = threadIdx.x;
-  const int64_t stride = gridDim.x;
-  int64_t pos = blockIdx.x;
-  if (pos >= npos) return;
-  // thread q < 32: predecessor (q < 16) or candidate (q >= 16) id q of position p
-  auto load_id = [&](int64_t p) -> int32_t {
-    const int64_t b = p / L, t = p % L;
-    const int32_t v = tid < kTopK ? (t == 0 ? last_verified[b] : cand_idx[(p - 1) * kTopK + tid])
-                                  : cand_idx[p * kTopK + tid - kTopK];
-    return clamp_token(v, V, err);
-  };
-  if (tid < 2 * kTopK) ids[0][tid] = load_id(pos);
-  int32_t next_id = tid < 2 * kTopK && pos + stride < npos ? load_id(pos + stride) : 0;
-  __syncthreads();
-  PairStage<KS> st;
-  pair_issue<KS>(st, ids[0], A, Bt, gpart, npos, pos, tid);
-  int buf = 0;
-  for (; pos < npos; pos += stride) {
-    const int64_t pn = pos + stride;
-    pair_gate<KS>(st, Pb, Hs, b_H, gate, pos, tid);
-    pair_store<KS>(st, Hs, G, Bc, tid);
-    if (tid < 2 * kTopK) ids[buf ^ 1][tid] = next_id;
-    next_id = tid < 2 * kTopK && pn + stride < npos ? load_id(pn + stride) : 0;
-    __syncthreads();   // G, Bc and the next position's ids are in place
-    if (pn < npos) pair_issue<KS>(st, ids[buf ^ 1], A, Bt, gpart, npos, pn, tid);
-    pair_products(G, Bc, cand_val, S, pos, tid);
-    __syncthreads();   // G and Bc are free again
-    buf ^= 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* base = pair_smem + static_cast<size_t>(warp) * pair_warp_bytes(KS);
+  uint16_t* As = reinterpret_cast<uint16_t*>(base);                  // [16][kRowPitch]
+  uint16_t* Bs = As + kTopK * kRowPitch;                              // [16][kRowPitch]
+  float* Ps = reinterpret_cast<float*>(Bs + kTopK * kRowPitch);       // [KS][256]
+  float* Hs = Ps + KS * kEmbed;                                       // [256]
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kPairWarps;
+  const int g = lane >> 2, c = lane & 3;
+  for (int64_t pos = static_cast<int64_t>(blockIdx.x) * kPairWarps + warp; pos < npos; pos += nwarps) {
+    const int64_t b = pos / L, t = pos - b * L;
+    // lane q: predecessor id q (q < 16; the last verified token at t = 0) or candidate id q - 16
+    int32_t id = lane < kTopK ? (t == 0 ? last_verified[b] : cand_idx[(pos - 1) * kTopK + lane])
+                              : cand_idx[pos * kTopK + lane - kTopK];
+    id = clamp_token(id, V, err);
+    __syncwarp();   // the previous position's reads of this warp's buffers are done
+    // row q: 32 16-byte pieces, lane = piece
+#pragma unroll 4
+    for (int q = 0; q < 2 * kTopK; ++q) {
+      const int32_t rid = __shfl_sync(0xFFFFFFFFu, id, q);
+      const uint16_t* src = (q < kTopK ? A : Bt) + static_cast<int64_t>(rid) * kEmbed + lane * 8;
+      cp_async16((q < kTopK ? As + q * kRowPitch : Bs + (q - kTopK) * kRowPitch) + lane * 8, src);
+    }
+    // the position's gate partials ([KS][256], split-major)
+#pragma unroll
+    for (int k = 0; k < KS * 2; ++k) {
+      const int item = lane + 32 * k;   // float4 item: split item / 64, piece item % 64
+      cp_async16(Ps + item * 4, gpart + ((item >> 6) * npos + pos) * kEmbed + (item & 63) * 4);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    // H_t = sigmoid(sum of the KS partials in split order + b_H): lane owns channels 8 lane .. 8 lane + 7
+    {
+      float o[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 z = *reinterpret_cast<const float4*>(Ps + lane * 8 + h * 4);
+#pragma unroll
+        for (int q = 1; q < KS; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(Ps + q * kEmbed + lane * 8 + h * 4);
+          z.x += v.x;
+          z.y += v.y;
+          z.z += v.z;
+          z.w += v.w;
+        }
+        const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = lane * 8 + h * 4 + j;
+          o[h * 4 + j] = 1.0f / (1.0f + expf(-(zz[j] + (b_H ? b_H[ch] : 0.0f))));
+        }
+      }
+      *reinterpret_cast<float4*>(Hs + lane * 8) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(Hs + lane * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      *reinterpret_cast<float4*>(gate + pos * kEmbed + lane * 8) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(gate + pos * kEmbed + lane * 8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
+    __syncwarp();
+    // the products: S (16 x 16) = G (16 x 256) B^T, two 8-column tiles
+    float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = ((lane >> 4) & 1) * 8;
+    const int brow = (lane & 7) + ((lane >> 4) & 1) * 8, bcol = ((lane >> 3) & 1) * 8;
+#pragma unroll 4
+    for (int kk = 0; kk < kEmbed / 16; ++kk) {
+      uint32_t af[4], bf[4];
+      ldmatrix_x4(af, As + arow * kRowPitch + kk * 16 + acol);
+      ldmatrix_x4(bf, Bs + brow * kRowPitch + kk * 16 + bcol);
+      const float2 h01 = *reinterpret_cast<const float2*>(Hs + kk * 16 + 2 * c);
+      const float2 h89 = *reinterpret_cast<const float2*>(Hs + kk * 16 + 2 * c + 8);
+      uint32_t ahi[4], alo[4];
+      scale_split(af[0], h01.x, h01.y, ahi[0], alo[0]);
+      scale_split(af[1], h01.x, h01.y, ahi[1], alo[1]);
+      scale_split(af[2], h89.x, h89.y, ahi[2], alo[2]);
+      scale_split(af[3], h89.x, h89.y, ahi[3], alo[3]);
+      mma_bf16(acc[0], ahi, bf[0], bf[1]);
+      mma_bf16(acc[0], alo, bf[0], bf[1]);
+      mma_bf16(acc[1], ahi, bf[2], bf[3]);
+      mma_bf16(acc[1], alo, bf[2], bf[3]);
+    }
+    // S[i][j] = U_j + acc: rows g and g + 8, columns 8 nt + 2 c, + 1
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int j = nt * 8 + 2 * c;
+      const float2 u = make_float2(cand_val[pos * kTopK + j], cand_val[pos * kTopK + j + 1]);   // 4-byte aligned only
+      *reinterpret_cast<float2*>(S + (pos * kTopK + g) * kTopK + j) = make_float2(u.x + acc[nt][0], u.y + acc[nt][1]);
+      *reinterpret_cast<float2*>(S + (pos * kTopK + g + 8) * kTopK + j) =
+          make_float2(u.x + acc[nt][2], u.y + acc[nt][3]);
+    }
   }
 }
 
@@ -222,10 +220,24 @@ cudaError_t launch_pair_scores(const int32_t* cand_idx, const float* cand_val,
                                float* S, uint32_t* err, int num_sms, cudaStream_t stream) {
   const int64_t npos = B * L;
   const int ks = gate_plan(npos, d, num_sms).ks;
-  const int64_t slots = static_cast<int64_t>(kPairCtasPerSm) * num_sms;
+  const int64_t ctas = (npos + kPairWarps - 1) / kPairWarps;
+  const size_t smem = kPairWarps * pair_warp_bytes(8);
+  cudaError_t se;
+  switch (ks) {
+    case 1: se = set_smem_limit<pair_kernel<1>>(smem); break;
+    case 2: se = set_smem_limit<pair_kernel<2>>(smem); break;
+    case 3: se = set_smem_limit<pair_kernel<3>>(smem); break;
+    case 4: se = set_smem_limit<pair_kernel<4>>(smem); break;
+    case 5: se = set_smem_limit<pair_kernel<5>>(smem); break;
+    case 6: se = set_smem_limit<pair_kernel<6>>(smem); break;
+    case 7: se = set_smem_limit<pair_kernel<7>>(smem); break;
+    default: se = set_smem_limit<pair_kernel<8>>(smem); break;
+  }
+  if (se != cudaSuccess) return se;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(npos < slots ? npos : slots), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas < num_sms ? ctas : num_sms), 1, 1);
+  cfg.blockDim = dim3(kPairWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = kPairWarps * pair_warp_bytes(ks);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
