@@ -88,15 +88,16 @@ _PROFILED = {
     "pairs": ["gate_gemm_B128_d5120.md", "pair_kernel_B128.md"],
     "verify0": ["verify_kernel_T0_B128.md"],
     "verify1": ["verify_kernel_T1_B128.md"],
+    "walk0": ["walk_T0_B128.md"],
     "walk1": ["walk_T1_B128.md"],
 }
 _SOURCES = {
     "topk16": ["topk.cu", "common.cuh"],
     "conv2tap": ["conv2tap.cu", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
     "verify": ["verify.cu", "common.cuh", "philox.cuh"],
-    "pair_scores": ["select.cu", "pair_math.cuh", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
+    "pair_scores": ["select.cu", "gemm_pair.cuh", "tcgen05.cuh", "common.cuh"],
     "proj": ["proj.cu", "pair_math.cuh", "tcgen05.cuh", "common.cuh"],
-    "walk": ["walk.cu", "common.cuh", "philox.cuh"],
+    "walk": ["walk.cu", "common.cuh", "philox.cuh", "exp2.cuh"],
     "lmhead": ["lmhead.cu", "tcgen05.cuh", "common.cuh"],
     "viterbi": ["viterbi.cu", "common.cuh"],
     "eval": ["eval.cu", "common.cuh"],
@@ -105,7 +106,7 @@ _SOURCES = {
 _PROFILE_SOURCES = {"conv2tap_B128_d5120.md": "conv2tap", "topk16_B128_V151936.md": "topk16",
                     "gate_gemm_B128_d5120.md": "pair_scores", "pair_kernel_B128.md": "pair_scores",
                     "verify_kernel_T0_B128.md": "verify", "verify_kernel_T1_B128.md": "verify",
-                    "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead",
+                    "walk_T0_B128.md": "walk", "walk_T1_B128.md": "walk", "lmhead_M1024_V151936_d5120.md": "lmhead",
                     "walk_viterbi_B16384.md": "viterbi", "selector_eval_B524288.md": "eval",
                     "proj_kernel_B128_d5120.md": "proj", "gemm_conv_kernel_B128_K5120_d5120.md": "gemm_conv"}
 
