@@ -923,7 +923,7 @@ def _repeat(fn, repeats):
     return ts
 
 
-def run_cpu_baseline(w, target_bits, sample_all=64, sample_one=4, repeats=3, lm_rows_all=16, lm_rows_one=1):
+def run_cpu_baseline(w, target_bits, sample_all=64, sample_one=4, repeats=3, lm_rows_all=64, lm_rows_one=2):
     """The oracle as it stands on the host cores: the full cycle on a sample of the
     workload's sequences, all cores and one thread, several repeats each; and the
     LM head + top-16 oracle's time per row on the C4 shapes (d=5120, V=151936)."""
