@@ -134,6 +134,9 @@ int dflash2_topk(dflash2_handle* h, const uint16_t* logits, int64_t rows, int64_
  *                       split-K partials, rewritten by every call; calls that overlap
  *                       on the GPU must not share it.  The partials are summed in a
  *                       fixed order, so H has the same bits on every call.
+ * Precision: the sum over q accumulates in fp32 on the tensor cores; each
+ * product A[p_i,q] H[b,t,q] (an fp32 value) enters as its bf16 rounding plus the
+ * bf16 rounding of the remainder, which carries it to about 2^-16 of its size.
  * d % 64 == 0, L <= 64.  Ids outside [0, V) are clamped and flagged.  A too-small
  * or NULL workspace returns DFLASH2_ERR_WORKSPACE.
  */
