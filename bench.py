@@ -998,8 +998,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="dflash2", choices=["dflash2", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
