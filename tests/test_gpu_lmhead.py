@@ -8,6 +8,7 @@ states.  GPU values are within 1e-3 (abs + rel) of the exact fp64 logits of
 the same ids."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from draft_selection_dflash2_gb300 import api, synth
@@ -67,3 +68,40 @@ def test_lmhead_workspace_too_small(handle):
     with pytest.raises(api.Dflash2Error) as e:
         api.lmhead_topk(handle, hid, W, workspace=ws)
     assert e.value.status == -7
+
+
+def test_lmhead_feeds_pair_scores_and_walk(handle):
+    # The fused head's candidates feed the selector as B sequences of L
+    # positions.  Each position's 16 best tokens are planted (W rows along its
+    # hidden state, logits a_j |h|^2 with a_j spaced so the gaps are ~1.3),
+    # so both sides pick the same ids in the same order; each side then runs
+    # its own pair scores and greedy walk.
+    B, L, V, d = 4, 16, 4096, 512
+    M = B * L
+    rng = np.random.default_rng(17)
+    hid = synth.normal_bits(40, (M, d))
+    hf = synth.bf16_to_f32(hid).astype(np.float32)
+    Wf = (rng.standard_normal((V, d)) * 0.01).astype(np.float32)
+    alpha = 0.05 * (1.0 - np.arange(K) / 20.0)
+    for m in range(M):
+        for j in range(K):
+            Wf[m * K + j] = hf[m] * np.float32(alpha[j])
+    W = synth.bf16_bits(Wf)
+    vals, idx = api.lmhead_topk(handle, bf(hid), bf(W))
+    ov, oi = oracle.lmhead_topk(hid, W, np.arange(M, dtype=np.int64), k=K)
+    assert np.array_equal(host(idx), oi)
+    W_H = synth.normal_bits(41, (256, d), std=0.02)
+    A = synth.normal_bits(42, (V, 256), std=0.02)
+    Bt = synth.normal_bits(43, (V, 256), std=0.02)
+    lv = rng.integers(0, V, B).astype(np.int32)
+    ci = idx.view(B, L, K)
+    S, gate = api.pair_scores(handle, ci, vals.view(B, L, K), torch.from_numpy(lv).cuda(), bf(hid).view(B, L, d),
+                              bf(W_H), None, bf(A), bf(Bt))
+    H = oracle.gate(hid, W_H, None)
+    oS, _ = oracle.pair_scores(oi.reshape(B, L, K), ov.reshape(B, L, K), lv, H.reshape(B, L, 256), A, Bt)
+    gS = host(S).astype(np.float64)
+    assert np.all(np.abs(gS - oS) <= 1e-4 + 1e-3 * np.abs(oS))
+    tok, slot, _ = api.walk(handle, S, ci)
+    otok, oslot, _, _ = oracle.walk(oS.astype(np.float32), oi.reshape(B, L, K))
+    assert np.array_equal(host(slot), oslot) and np.array_equal(host(tok), otok)
+    assert handle.device_error() == 0
