@@ -25,7 +25,8 @@ def run_case(h, sel, logits_bits=None):
 @pytest.mark.parametrize("B,L,V,d,emb", [(1, 8, 4096, 512, 0.02), (1, 8, 4096, 512, 0.25),
                                          (3, 5, 4096, 512, 0.25), (1, 16, 151936, 2560, 0.02),
                                          (8, 16, 151936, 5120, 0.25), (16, 16, 4096, 2560, 0.25),
-                                         (48, 16, 8192, 5120, 0.02)])
+                                         (48, 16, 8192, 5120, 0.02), (2, 1, 4096, 512, 0.25),
+                                         (96, 16, 8192, 512, 0.25)])
 def test_pair_scores_match_oracle(handle, B, L, V, d, emb):
     sel = synth.selector_inputs(B * 100 + L, B, L, V, d, emb_std=emb)
     S, gate, oS, H, bad = run_case(handle, sel)
