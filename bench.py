@@ -226,6 +226,17 @@ def to_dev(torch, a, dev):
     return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
 
 
+LEAD_CYCLES = 4_000_000   # ~2 ms of device clock at 2 GHz
+
+
+def device_lead(torch):
+    """Queue a device-side wait (a clock spin of LEAD_CYCLES) ahead of a timed
+    region, so that the host has enqueued the timed launches before the first
+    event fires: the events then time the device's work, not the host's launch
+    latency.  The wait itself lies before the first event."""
+    torch.cuda._sleep(LEAD_CYCLES)
+
+
 class Cycle:
     """Device buffers and the step of the full cycle, through the Python API."""
 
@@ -329,9 +340,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    device_lead(torch)
     t0.record(stream)
+    host0 = time.perf_counter()
     for i in range(args.steps):
         cyc.step(seed_offset=1000 + i)
+    host_ms = (time.perf_counter() - host0) * 1e3 / args.steps
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -342,6 +356,7 @@ def run_gpu(args):
     # the stage breakdown: the same steps again with an event between stages (an
     # event between two kernels stops the next one from starting early, so the
     # timed pass above records none)
+    device_lead(torch)
     for i in range(args.steps):
         cyc.step(ev=evs[i], seed_offset=1000 + i)
     torch.cuda.synchronize()
@@ -397,6 +412,10 @@ def run_gpu(args):
         "roofline": roofline,
         "clocks": clk,
         "gpu_launches": cyc.launches_per_step * args.steps,
+        "host_enqueue_ms_per_step": round(host_ms, 4),
+        "timing": "CUDA events on the launching stream; a device-side wait queued before the first event lets "
+                  "the host enqueue ahead, so the interval is the device's (host_enqueue_ms_per_step below "
+                  "ms_per_step: the device never waited for the host)",
     }
 
     if rank == 0 and args.sweep:
@@ -459,6 +478,7 @@ def run_sweep(torch, api, h, w, cyc, dev, pk, logits="planted"):
         for it in range(steps + 3):
             flush.zero_()   # L2 flush (buffer larger than L2)
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            device_lead(torch)
             e[0].record()
             api.topk(h, U, vals=vals, idx=idx)
             e[1].record()
@@ -565,6 +585,7 @@ def run_small_cycles(torch, api, h, dev):
             g.replay()
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            device_lead(torch)
             a.record()
             for _ in range(reps):
                 g.replay()
@@ -629,6 +650,7 @@ def _timed(torch, fn, reps=5, warm=2):
     ts = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        device_lead(torch)
         a.record()
         fn()
         b.record()

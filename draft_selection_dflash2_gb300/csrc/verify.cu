@@ -8,15 +8,18 @@
 // (first_reject[b] only falls, so a row past it stays dead).  Rows are taken
 // position-major, the sequence fastest.
 //
-// T = 0, one cooperative launch (all CTAs resident): each target row is cut
-//   into contiguous chunks of about 4096 ids, one warp's item, and the (t,
-//   chunk, b) items are strided over all warps of the grid.  A warp checks its
-//   next 32 items' liveness at once, with the loads of the first already in
-//   flight, and skips the dead ones.  The row's arg-max key (value order, then
-//   lowest id) is kept by a 64-bit atomic max per row; a chunk holding a key
-//   above the draft token's rejects the row at once (atomicMin on
-//   first_reject), so no chunk waits for another.  After a grid barrier, row
-//   n's key gives its token.
+// T = 0, one cooperative launch of the co-resident grid (no CTA waits for
+//   another: the cooperative launch is kept for where it places the CTAs --
+//   a plain launch of the same grid lands them on the SMs in another order and
+//   measured 11% slower): each target row is cut into contiguous chunks of about
+//   4096 ids, one warp's item, and the (t, chunk, b) items are strided over
+//   all warps of the grid.  A warp checks its next 32 items' liveness at once,
+//   with the loads of the first already in flight, and skips the dead ones.
+//   The row's arg-max key (value order, then lowest id) is kept by a 64-bit
+//   atomic max per row; a chunk holding a key above the draft token's rejects
+//   the row at once (atomicMin on first_reject), so no chunk waits for
+//   another.  The last CTA to finish (a counter raised after a fence) reads
+//   row n's key for its token and writes the outputs; no CTA waits for another.
 //
 // T > 0, the target distribution in exact fixed point: with c = log2(e) / T
 //   and M the row's largest non-NaN logit, every id weighs
@@ -409,44 +412,13 @@ struct VerifyArgs {
   uint32_t* decided;            // T > 0: 1 once the row's accept test is done
   unsigned long long* slices;   // T > 0: [rows, 8] slice weight sums
   unsigned long long* runs;     // T > 0: [rows, 8, 16] warp-run weight sums
-  unsigned* bar;           // T = 0: [0] count, [1] generation, [2] abort
+  unsigned* bar;           // T = 0: [0] the count of CTAs done
   uint32_t* err;
 };
 
 // ===========================================================================
 // T = 0
 // ===========================================================================
-// Sense by generation: the last CTA to arrive resets the count and bumps the
-// generation.  A wait that passes kWaitLimitNs raises DFLASH2_DEVERR_TIMEOUT and
-// sets the shared abort word, after which every CTA leaves.
-__device__ void grid_barrier(unsigned* count, volatile unsigned* gen, volatile unsigned* abort_word, int& abort_flag,
-                             uint32_t* err) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned g = *gen;
-    __threadfence();
-    if (atomicAdd(count, 1u) == gridDim.x - 1) {
-      *count = 0u;
-      __threadfence();
-      *gen = g + 1;
-    } else {
-      const uint64_t start = global_timer_ns();
-      while (*gen == g) {
-        if (*abort_word) break;
-        __nanosleep(64);
-        if (global_timer_ns() - start > kWaitLimitNs) {
-          raise_error(err, DFLASH2_DEVERR_TIMEOUT);
-          *abort_word = 1u;
-          break;
-        }
-      }
-    }
-    __threadfence();
-    abort_flag = *abort_word ? 1 : 0;
-  }
-  __syncthreads();
-}
-
 // A work item's (position, sequence, chunk).
 struct ItemPos {
   int t, b, ch;
@@ -474,19 +446,18 @@ __global__ void verify_init_kernel(int32_t* first_reject, unsigned long long* ro
   if (i < B) first_reject[i] = static_cast<int32_t>(L);
   if (!sampled && i < rows) rowval[i] = 0ull;
   if (sampled && i < rows) decided[i] = 0u;
-  if (i < 4) bar[i] = 0u;   // count, generation, abort
+  if (i < 4) bar[i] = 0u;   // the T = 0 count (and three spare words)
 }
 
 __global__ void __launch_bounds__(kVThreads, kVCtasPerSm) verify_greedy_kernel(const VerifyArgs a) {
-  __shared__ int abort_flag;
-  pdl_launch_dependents();   // launched in full order after its init kernel; lets the next kernel prepare
+  __shared__ int last_cta;
+  pdl_wait();   // no-op: a cooperative launch starts after the init kernel completes
+  pdl_launch_dependents();   // lets the next kernel prepare
   const int64_t B = a.B, L = a.L, V = a.V;
   const int nch = verify_chunks(V);
   const int64_t cs = verify_chunk_ids(V);
   volatile int32_t* fr = a.first_reject;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) abort_flag = 0;
-  __syncthreads();
   {
     // item = (t * nch + ch) * B + b: position-major, the sequence fastest, so a
     // sequence's chunks fall on warps of different CTAs (and SMs) and the work
@@ -544,12 +515,20 @@ __global__ void __launch_bounds__(kVThreads, kVCtasPerSm) verify_greedy_kernel(c
       }
       cur = item_add(cur, stride, nch, Bi);
     }
-    grid_barrier(a.bar, a.bar + 1, a.bar + 2, abort_flag, a.err);
   }
-  if (abort_flag) return;   // a barrier gave up: DFLASH2_DEVERR_TIMEOUT is raised
+  // Every thread's atomics are ordered before its CTA's count by fences; the
+  // CTA that brings the count to gridDim.x has seen all of them.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last_cta = atomicAdd(a.bar, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (!last_cta) return;
+  __threadfence();
   // n = first_reject[b]: the accepted prefix, row n's token, then -1
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < B; b += stride) {
+  for (int64_t b = threadIdx.x; b < B; b += blockDim.x) {
     const int32_t n = fr[b];
     for (int64_t t = 0; t <= L; ++t) {
       if (t < n) {

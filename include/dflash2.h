@@ -315,7 +315,7 @@ int dflash2_gemm_conv2tap(dflash2_handle* h, const uint16_t* A, const uint16_t* 
  *   cand_idx    device int32 [B, L, 16]
  *   accept_len  device int32 [B];  out_tok device int32 [B, L+1]
  *   workspace   device scratch of at least dflash2_verify_workspace(h, B, L, V)
- *               bytes, 256-byte aligned (barrier words, per-row counters, maxima
+ *               bytes, 256-byte aligned (counter words, per-row counters, maxima
  *               and sums, per-chunk sums), fully re-initialised by every call;
  *               calls that overlap on the GPU must not share it.
  * draft_q, draft_slot and cand_idx may be NULL when temperature <= 0, and every
