@@ -27,13 +27,15 @@
 //   Z = sum_v W_v.  Integer sums are the same in any order, so partial sums
 //   over slices give the exact Z and exact prefix sums.
 //   verify_rows_kernel: one thread-block cluster of 8 CTAs per row.  Each CTA
-//   copies its eighth of the row into shared memory with bulk copies (TMA,
-//   completing on an mbarrier; the next row's slice is requested while this
-//   row is summed, into the other of two buffers), takes its maximum, and the
-//   8 maxima meet in distributed shared memory (cluster barrier); each CTA
-//   then sums its slice's weights from shared memory, the 8 sums meet in CTA
-//   0, which runs the accept test (u1 q) Z < W_x in fp64 and lowers
-//   first_reject[b] on a rejection.  Clusters never wait for one another.
+//   copies its eighth of the row into shared memory with one bulk copy (TMA,
+//   completing on an mbarrier; the next row's copy is requested once this
+//   row is done), takes its maximum, and the 8 maxima meet in distributed
+//   shared memory (cluster barrier); each CTA then sums its slice's weights
+//   from shared memory, the 8 sums meet in CTA 0, which runs the accept test
+//   (u1 q) Z < W_x in fp64, lowers first_reject[b] on a rejection and marks
+//   the row decided.  A cluster takes a row only once the row before it in the
+//   sequence is decided (a bounded wait on that flag), so nothing is read on
+//   speculation.
 //   verify_draw_kernel (one CTA per sequence): the token of row n =
 //   first_reject[b] by inverse CDF in id order over integer prefix sums --
 //   from the residual max(0, W_v - Q_v), Q_v = floor(q_v Z), after a rejection,
