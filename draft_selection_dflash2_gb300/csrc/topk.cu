@@ -2,7 +2,7 @@
 // Parallel", "A Lightweight Path Selector": keep the top 16 candidates of the
 // drafter's own logits at every block position).
 //
-// Two forms.  Segments of up to kHistSegMax logits (rows up to 393,216 per
+// Two forms.  Segments of up to kHistSegMax logits (rows up to 196,608 per
 // CTA, longer ones split over a larger cluster first) take the group-maximum
 // form below (topk16_hist_kernel); longer segments take the running-threshold
 // stream (topk16_kernel):
@@ -324,22 +324,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
 // Group-maximum form (segments up to kHistSegMax logits)
 // ---------------------------------------------------------------------------
 // A thread's 8 vectors of one CTA iteration (64 logits) form a group.  The
-// stream keeps only each group's maximum (in shared memory), so a lane's
-// vector is dead once its maximum is taken and its next load is issued at
-// once: the stream runs at close to a plain copy's read rate.  Then
-// T = the 16th largest of the 256 threads' maxima: those are 16 distinct
+// stream keeps for each group (in shared memory) its maximum, where it sits
+// (vector and element) with its bits, and the largest of the group's other 63
+// logits; a lane's vector is dead once these are updated and its next load is
+// issued at once, so the stream runs at close to a plain copy's read rate.
+// Then T = the 16th largest of the 256 threads' maxima: those are 16 distinct
 // logits >= T, so no logit below T is in the segment's top-16, and every
-// logit of the top-16 lies in a group whose maximum reaches T.  Only those
-// groups (about 16 of a row's 2,400) are read again, by the thread that
-// streamed them (from L2, as a rule), their logits >= T keyed exactly and
-// folded into the warp lists; the segment's few trailing logits (V % 8) are
-// keyed directly.  Rows of ties (every group reaching T) stay exact: the
-// folds take any number of keys.
-constexpr int kHistIters = 24;                                        // CTA iterations a segment may take
+// logit of the top-16 lies in a group whose maximum reaches T (about 16 of a
+// row's 2,400).  A group whose other logits all fall below T holds exactly one
+// logit >= T, keyed from the history alone; any other reaching group is read
+// again by the thread that streamed it (from L2, as a rule) and its logits
+// >= T keyed exactly.  The keys fold into the warp lists; the segment's few
+// trailing logits (V % 8) are keyed directly.  Rows of ties (every group
+// reaching T) stay exact: their groups are read again, and the folds take any
+// number of keys.
+constexpr int kHistIters = 12;                                        // CTA iterations a segment may take
 constexpr int64_t kHistSegMax = static_cast<int64_t>(kHistIters) * kThreads * kUnroll * 8;
 
+// A group's history entry (0: the thread had no data in that iteration):
+//   bits  0..16  bf16 order of the group maximum + 1
+//   bits 17..22  where the maximum sits: 8 * vector + element (its first
+//                occurrence in the vector that first holds it)
+//   bits 23..38  the maximum's own bf16 bits
+//   bits 39..54  bf16 order of the largest of the other 63 logits (an upper
+//                bound when some are NaN)
+//   bit  55      the maximum was located (the group holds a non-NaN logit)
+constexpr int kHistMaxBits = 17;
+
 struct HistSmem {
-  uint32_t hist[kHistIters][kThreads];   // 0: no data; else bf16 order of the group maximum + 1
+  uint64_t hist[kHistIters][kThreads];
   uint64_t cand[kWarps][kWarpCap];
   uint64_t warp_top[kWarps][kTopK];
   uint64_t top[kTopK];
@@ -379,31 +392,67 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
   if (tid < kWarps) s.wcount[tid] = 0;
   if (tid == 0) s.gthr = 0ull;
 
-  // ---- stream: group maxima; a lane reloads each vector as soon as it is reduced
+  // ---- stream: group histories; a lane reloads each vector as soon as it is reduced
   const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);   // never a maximum
+  const __nv_bfloat16 ninf = __ushort_as_bfloat16(static_cast<unsigned short>(0xFF80u));
   uint4 v[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int64_t vi = u * stride + tid;
     v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : nan4;
   }
-  uint32_t lane_max = 0u;   // the largest of this thread's group entries
+  uint32_t lane_max = 0u;   // the largest of this thread's group maxima (order + 1)
   for (int it = 0; it < iters; ++it) {
     const int64_t nb = static_cast<int64_t>(it + 1) * per_iter;
     uint32_t m2 = 0u;
+    // the first vector holding the largest vector maximum (NaN taken as -inf
+    // here), the vector itself, and the largest maximum of the other vectors
+    __nv_bfloat16 best = ninf, rest = ninf;
+    int bu = 0;
+    uint4 bv = v[0];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t w = max2_bits(max2_bits(v[u].x, v[u].y), max2_bits(v[u].z, v[u].w));
       m2 = u == 0 ? w : max2_bits(m2, w);
+      const __nv_bfloat162 wb = *reinterpret_cast<const __nv_bfloat162*>(&w);
+      const __nv_bfloat16 vm = __hmax(__hmax(__low2bfloat16(wb), __high2bfloat16(wb)), ninf);
+      if (u == 0) {
+        best = vm;
+      } else {
+        const bool better = __hgt(vm, best);
+        rest = __hmax(rest, better ? best : vm);
+        best = better ? vm : best;
+        bu = better ? u : bu;
+        bv = better ? v[u] : bv;
+      }
       const int64_t vi = nb + u * stride + tid;
       v[u] = vi < n_vecs ? ldg_stream(seg + vi * 8) : nan4;
     }
     const __nv_bfloat162 mb = *reinterpret_cast<const __nv_bfloat162*>(&m2);
     const uint32_t gm = __bfloat16_as_ushort(__hmax(__low2bfloat16(mb), __high2bfloat16(mb)));
     const bool has = static_cast<int64_t>(it) * per_iter + tid < n_vecs;
-    const uint32_t h = has ? bf16_order(gm) + 1u : 0u;
+    uint64_t h = has ? bf16_order(gm) + 1u : 0u;
+    if (has && bf16_order(gm) != 0u) {
+      // the maximum's first element in its vector; the largest of the vector's others
+      int k0 = -1;
+      __nv_bfloat16 other = ninf;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const __nv_bfloat16 e = __ushort_as_bfloat16(static_cast<unsigned short>(lane_elem(bv, k)));
+        const bool hit = k0 < 0 && __heq(e, best);
+        other = hit ? other : __hmax(other, e);
+        k0 = hit ? k : k0;
+      }
+      if (k0 >= 0) {
+        const uint32_t mbits = lane_elem(bv, k0);
+        const uint32_t rest_ord = bf16_order(__bfloat16_as_ushort(__hmax(rest, other)));
+        h |= (static_cast<uint64_t>(bu * 8 + k0) << kHistMaxBits) | (static_cast<uint64_t>(mbits) << 23) |
+             (static_cast<uint64_t>(rest_ord) << 39) | (1ull << 55);
+      }
+    }
     s.hist[it][tid] = h;
-    lane_max = h > lane_max ? h : lane_max;
+    const uint32_t hm = static_cast<uint32_t>(h) & ((1u << kHistMaxBits) - 1u);
+    lane_max = hm > lane_max ? hm : lane_max;
   }
 
   // ---- T: the 16th largest thread maximum (the maxima of 16 threads are 16
@@ -431,15 +480,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
   const __nv_bfloat162 t2 = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(tb)),
                                                __ushort_as_bfloat16(static_cast<unsigned short>(tb)));
 
-  // ---- the groups that reach T, read again and keyed exactly; each thread
-  // fetches its own, so a warp's first round covers the usual single group
+  // ---- the groups that reach T: keyed from the history when they hold one
+  // logit >= T, else read again and keyed exactly; each thread takes its own,
+  // one group per round, so a warp's first round covers the usual single group
   WarpSel w{0ull, 0ull};
   uint64_t* cand = s.cand[warp];
   int* wcount = &s.wcount[warp];
   auto next_sel = [&](int from) {
     int it = from;
     if (lane_max >= T)
-      while (it < iters && s.hist[it][tid] < T) ++it;
+      while (it < iters && (static_cast<uint32_t>(s.hist[it][tid]) & ((1u << kHistMaxBits) - 1u)) < T) ++it;
     else
       it = iters;
     return it;
@@ -447,13 +497,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
   int it = next_sel(0);
   while (__ballot_sync(0xFFFFFFFFu, it < iters) != 0u) {
     const bool sel = it < iters;
-    const int64_t b0 = static_cast<int64_t>(sel ? it : 0) * per_iter + tid;
+    const uint64_t hist = sel ? s.hist[it][tid] : 0ull;
+    // one logit >= T (t_ord > 0: NaN never reaches it): the located maximum
+    const bool lone = sel && t_ord != 0u && ((hist >> 55) & 1ull) && ((hist >> 39) & 0xFFFFull) < t_ord;
+    if (lone) {
+      const int pos = static_cast<int>((hist >> kHistMaxBits) & 63ull);
+      const int64_t vi = static_cast<int64_t>(it) * per_iter + (pos >> 3) * stride + tid;
+      const uint64_t key = make_key(static_cast<uint32_t>((hist >> 23) & 0xFFFFull),
+                                    static_cast<uint32_t>(seg_begin + vi * 8 + (pos & 7)));
+      if (key > w.thr) cand[atomicAdd(wcount, 1)] = key;
+    }
+    __syncwarp();
+    if (*reinterpret_cast<volatile int*>(wcount) > kFoldAt) fold_warp(w, cand, wcount, &s.gthr, lane);
+    const bool reread = sel && !lone;
+    const int64_t b0 = static_cast<int64_t>(reread ? it : 0) * per_iter + tid;
     uint4 x[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) x[u] = sel && b0 + u * stride < n_vecs ? ldg_stream(seg + (b0 + u * stride) * 8) : nan4;
+    for (int u = 0; u < kUnroll; ++u) x[u] = reread && b0 + u * stride < n_vecs ? ldg_stream(seg + (b0 + u * stride) * 8) : nan4;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (sel && b0 + u * stride < n_vecs) {
+      if (reread && b0 + u * stride < n_vecs) {
         const uint32_t id0 = static_cast<uint32_t>(seg_begin + (b0 + u * stride) * 8);
         uint32_t em = t_ord == 0u ? 0xFFu : elem_reach_mask(x[u], t2);
         while (em) {

@@ -104,7 +104,7 @@ def test_topk_edge_rows_on_the_whole_row_path(handle):
 @pytest.mark.parametrize("rows,V", [(3, 1_000_000), (2, 6_500_000)])
 def test_topk_long_rows(handle, rows, V):
     # V = 1M: each row is split over a cluster until a segment fits the group
-    # history (393,216 logits); V = 6.5M exceeds it even over 16 CTAs and
+    # history (196,608 logits); V = 6.5M exceeds it even over 16 CTAs and
     # takes the running-threshold stream
     rng = np.random.default_rng(V + rows)
     check(handle, synth.logits_planted(rng, rows, V))
