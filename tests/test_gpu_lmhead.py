@@ -48,6 +48,14 @@ def test_lmhead_small_ragged(handle):
     assert n > M // 2
 
 
+@pytest.mark.parametrize("M,V,d", [(500, 5000, 256), (1000, 3001, 128)])
+def test_lmhead_several_pairs_ragged(handle, M, V, d):
+    # 4 and 8 hidden-row tiles (the last one partial): two and four CTA pairs
+    # per vocabulary run; ragged last vocabulary tile
+    n = check(handle, M, V, d, rows=list(range(M)), w_std=0.1)
+    assert n > M // 2
+
+
 def test_lmhead_single_row(handle):
     check(handle, 1, 777, 128, rows=[0], w_std=0.1)
 
