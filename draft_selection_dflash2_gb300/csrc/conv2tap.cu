@@ -9,10 +9,11 @@
 //
 // Two kernels.
 //   1. The correction, a [M, d] x [d, 2G] contraction, on CTA pairs
-//      (gemm_pair.cuh): 256 positions x 2 BNG columns per pair tile, the tile's
-//      B operand stacking W_c rows [g0, g0 + BNG) (c0) and [G + g0, G + g0 +
-//      BNG) (c1) as two sub-blocks, K split ks ways; each split stores its fp32
-//      partial [M, 2G] to the workspace.
+//      (gemm_pair.cuh): 256 positions x 2 BNG columns per pair tile in one
+//      MMA per K step, whose B operand is W_c rows [g0, g0 + BNG) (c0, in CTA
+//      rank 0) and [G + g0, G + g0 + BNG) (c1, in rank 1), K split ks ways;
+//      each split stores its fp32 partial [M, 2G] to the workspace.  One MMA
+//      per K step reads the A tile once (two sub-block MMAs read it twice).
 //   2. The taps, a streaming pass (conv_tap_kernel): one thread per 8-channel
 //      unit walks the L positions of one sequence, carrying x_t over as the
 //      next position's x_{t-1} (x_prev at the first), and writes y with 16-byte
@@ -29,16 +30,19 @@
 namespace dflash2 {
 namespace {
 
-constexpr int kConvBNG = 160;       // groups per pair tile (two N = 160 MMAs)
+constexpr int kConvBNG = 128;       // groups per pair tile (one N = 256 MMA: c0 and c1 of 128 groups)
 constexpr int kTapThreads = 128;    // 8-channel units per CTA
 constexpr int kTapRows = 8;         // positions whose x a thread holds at once
 
 struct ConvShape {
-  static constexpr int kSubs = 2;
+  static constexpr int kSubs = 1;
   struct Params {
     int G, BNG;
   };
-  __device__ static int b_row(const Params& p, int n_tile, int sb) { return (sb ? p.G : 0) + n_tile * p.BNG; }
+  // rank 0 holds the c0 rows of the tile's groups, rank 1 their c1 rows (half = BNG)
+  __device__ static int b_row(const Params& p, int n_tile, int, int rank, int) {
+    return (rank ? p.G : 0) + n_tile * p.BNG;
+  }
   // tile columns [c, c + 4): c0 of groups g0 + c.., or c1 of groups g0 + c - BNG..
   // (BNG and G are multiples of 4, so the four are all valid or all not)
   __device__ static bool valid(const Params& p, int n_tile, int c) {
@@ -236,7 +240,7 @@ cudaError_t launch_conv2tap(const uint16_t* x, const uint16_t* x_prev, const uin
   const int G = static_cast<int>(d / 16);
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_2d(&ta, hs ? hs : x, M, d, d, 128) ||
-      !make_tmap_bf16_2d(&tb, W_c, 2 * G, d, d, static_cast<uint32_t>(cp.BNG / 2)))
+      !make_tmap_bf16_2d(&tb, W_c, 2 * G, d, d, static_cast<uint32_t>(cp.BNG)))
     return cudaErrorInvalidValue;
   float* part = static_cast<float*>(workspace);
   cudaError_t e = launch_pair_gemm<ConvShape>(ta, tb, cp.sh, ConvShape::Params{G, cp.BNG}, part, err, stream);

@@ -27,9 +27,10 @@
 //                TMA tensor store, double-buffered per warp.  Blocks that are
 //                only partly valid (ragged shapes) are stored by guarded float4
 //                writes instead.
-// The B tile is Shape::kSubs sub-blocks of BN / kSubs columns; sub-block s of
-// n-tile t takes B rows Shape::b_row(t, s) + rank * BN / kSubs / 2 in CTA
-// rank, and tile columns [c, c + 4) (c % 4 == 0) go to output columns
+// The B tile is Shape::kSubs sub-blocks of BN / kSubs columns; CTA rank holds
+// BN / kSubs / 2 of each sub-block's rows, from B row Shape::b_row(t, s, rank,
+// BN / kSubs / 2) on (sub-block s of n-tile t), and the pair MMA takes rank 0's
+// rows as the sub-block's first columns; tile columns [c, c + 4) (c % 4 == 0) go to output columns
 // Shape::out_col(t, c) + [0, 4) (or nowhere when Shape::valid(t, c) is false).
 // Every mbarrier wait is bounded (DFLASH2_DEVERR_TIMEOUT, then drain and exit).
 #pragma once
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kPgThreads, 1)
         pg_tma_load(a_dst, &tmA, kx, m0, bar, pol_a);
         for (int sb = 0; sb < Shape::kSubs; ++sb)
           pg_tma_load(a_dst + kPgABytes + sb * half * kTileRowBytes, &tmB, kx,
-                      Shape::b_row(sp, n_tile, sb) + static_cast<int>(rank) * half, bar, pol_b);
+                      Shape::b_row(sp, n_tile, sb, static_cast<int>(rank), half), bar, pol_b);
         issued = i + 1;
       }
       // before this CTA may exit: its own copies have landed (the leader's
