@@ -19,9 +19,11 @@ def run(h, c, hs=None, y_fp32=True):
 
 @pytest.mark.parametrize("B,L,d,bias", [(1, 16, 2560, False), (2, 5, 192, True), (8, 16, 5120, False),
                                         (3, 64, 512, True), (1, 1, 64, False), (16, 16, 2560, True),
-                                        (24, 16, 5120, False), (128, 16, 5120, True)])
+                                        (24, 16, 5120, False), (128, 16, 5120, True), (2, 16, 768, False),
+                                        (17, 16, 1536, True), (16, 16, 1024, False)])
 def test_conv_fp32_matches_oracle(handle, B, L, d, bias):
-    # (128, 16, 5120): the benchmark's shape, 32 tiles with the K loop split 4 ways
+    # (128, 16, 5120): the benchmark's shape, 8 row pairs x 3 group tiles with the K loop split 3
+    # ways; 768, 1536 and 1024 take one 128-group tile that is partly empty
     c = synth.conv_inputs(B * 13 + L, B, L, d, with_bias=bias)
     y = run(handle, c)
     oy = oracle.conv2tap(c.x, c.x_prev, c.k0, c.k1, c.W_c, b_c=c.b_c)
@@ -63,7 +65,7 @@ def test_conv_identity_on_gpu(handle):
 
 
 def test_conv_unsplit_large_batch_sampled(handle):
-    # B=512, L=16, d=5120: 64 row tiles x 2 column tiles fill the GPU without a K
+    # B=512, L=16, d=5120: 32 row pairs x 3 group tiles fill the GPU without a K
     # split, so each CTA reduces nothing and streams its own 128 rows; sequences
     # checked against the oracle one by one (each depends only on its own rows)
     B, L, d = 512, 16, 5120
