@@ -208,8 +208,10 @@ ConvPlan conv_plan(int64_t M, int64_t d, int slots) {
   ConvPlan cp;
   const int G = static_cast<int>(d / 16);
   // N = 2 BNG = 32, 64 or 256: the pair-MMA widths that the parity tests cover
-  // (a 96-group tile, N = 192, gave wrong rows in the second CTA of the pair)
-  cp.BNG = G <= 16 ? 16 : (G <= 32 ? 32 : kConvBNG);
+  // (a 96-group tile, N = 192, gave wrong rows in the second CTA of the pair).
+  // A single row pair (at most 256 positions) takes 32-group tiles: more pairs
+  // share W_c, which then dominates the bytes.
+  cp.BNG = G <= 16 ? 16 : ((G <= 32 || M <= 256) ? 32 : kConvBNG);
   PairGemmShape& sh = cp.sh;
   sh.M = static_cast<int>(M);
   sh.K = static_cast<int>(d);
