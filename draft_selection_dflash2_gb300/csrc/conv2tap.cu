@@ -103,7 +103,7 @@ struct TapParams {
 // Grid (ceil(units / kTapThreads), B): thread -> unit u of sequence b.  KS =
 // the number of K splits, so that a block's partial loads are all in flight
 // before the first is used.  Five CTAs per SM (96 registers a thread) keep the
-// benchmark's 640 CTAs in one wave on 152 SMs.
+// 640 CTAs of 128 sequences at d = 5120 in one wave on 152 SMs.
 template <int KS>
 __global__ void __launch_bounds__(kTapThreads, 5) conv_tap_kernel(const TapParams p) {
   const int u = blockIdx.x * kTapThreads + threadIdx.x;
