@@ -618,6 +618,15 @@ __device__ __forceinline__ uint64_t smem_run_sum(const uint16_t* buf, int64_t q0
   return acc;
 }
 
+// A cluster barrier whose release side is paid only by the threads that wrote
+// something another CTA reads after it: they fence at cluster scope, every
+// thread then arrives relaxed and waits with acquire.  (A full release arrive
+// from every thread costs several times more per row.)  Whole-CTA call.
+__device__ __forceinline__ void cluster_sync_writers(bool wrote) {
+  if (wrote) asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Row r = t B + b (position-major); whether it still matters.
 __device__ __forceinline__ bool row_live(int64_t r, int64_t B, const volatile int32_t* fr) {
   const int64_t t = r / B, b = r - t * B;
@@ -811,7 +820,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows_kernel
     }
     m = block_max_u32(m, s.red32);
     if (threadIdx.x == 0) s.max_part = m;
-    cluster.sync();   // #1: the slice maxima are in
+    cluster_sync_writers(threadIdx.x == 0);   // #1: the slice maxima are in
     if (threadIdx.x == 0) {
       uint32_t mo = 0u;
       for (int k = 0; k < kRowCluster; ++k) mo = max(mo, *cluster.map_shared_rank(&s.max_part, k));
@@ -852,7 +861,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows_kernel
       a.slices[r * kRowCluster + rank] = sum;
       *cluster.map_shared_rank(&s.sum_part[rank], 0) = sum;
     }
-    cluster.sync();   // #2: the slice sums are in rank 0
+    cluster_sync_writers(threadIdx.x == 0);   // #2: the slice sums are in rank 0
     if (rank == 0 && threadIdx.x < 32) {
       if (threadIdx.x == 0) {
         uint64_t Z = 0ull;
@@ -872,7 +881,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) verify_rows_kernel
       const int64_t nr = next_ready_row(r + ncl, ncl, R, B, fr, a.decided, a.err, threadIdx.x);
       if (threadIdx.x < kRowCluster) *cluster.map_shared_rank(&s.next_row, threadIdx.x) = nr;
     }
-    cluster.sync();   // #3: the next row is in
+    cluster_sync_writers(rank == 0 && threadIdx.x < kRowCluster);   // #3: the next row is in
     const int64_t nr = s.next_row;
     if (nr < R && np == 1) {
       int64_t p0, p1;
