@@ -159,6 +159,19 @@ __device__ __noinline__ void fold_warp(WarpSel& w, uint64_t* cand, int* wcount, 
   w.thr = own > g ? own : g;
 }
 
+// The barriers around a row's merge.  A one-CTA cluster needs only the CTA
+// barrier; a larger one arrives relaxed, the threads that wrote data another
+// CTA reads after the barrier fencing at cluster scope first, and waits with
+// acquire.  Whole-CTA call.
+__device__ __forceinline__ void merge_sync(unsigned nrank, bool wrote) {
+  if (nrank == 1) {
+    __syncthreads();
+    return;
+  }
+  if (wrote) asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint16_t* __restrict__ logits,
                                                           int64_t V, int64_t ld, int64_t seg_len,
                                                           float* __restrict__ vals,
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
   }
 
   // Merge the cluster's partial lists in distributed shared memory.
-  cluster.sync();
+  merge_sync(nrank, warp == 0 && lane < kTopK);
   if (rank == 0 && warp == 0) {
     uint64_t acc = lane < kTopK ? s.top[lane] : 0ull;
     for (unsigned r = 1; r < nrank; r += 2) {
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_kernel(const uint
       idx[row * kTopK + lane] = key_id(acc);
     }
   }
-  cluster.sync();
+  merge_sync(nrank, false);   // rank 0 has read every list before any CTA leaves
 }
 
 // ---------------------------------------------------------------------------
@@ -575,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
     if (lane < kTopK) s.top[lane] = acc;
   }
   // the cluster's lists meet in distributed shared memory
-  cluster.sync();
+  merge_sync(nrank, warp == 0 && lane < kTopK);
   if (rank == 0 && warp == 0) {
     uint64_t acc = lane < kTopK ? s.top[lane] : 0ull;
     for (unsigned r = 1; r < nrank; r += 2) {
@@ -592,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk16_hist_kernel(const
       idx[row * kTopK + lane] = key_id(acc);
     }
   }
-  cluster.sync();
+  merge_sync(nrank, false);   // rank 0 has read every list before any CTA leaves
 }
 }  // namespace
 
